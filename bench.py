@@ -1,0 +1,424 @@
+"""Benchmark of one serving step of the paged-KV attention forward on GB300.
+
+A step is one pass of the whole path over one synthetic batch:
+pka_cache_write of the new tokens, then pka_paged_attn_forward (planner,
+decode / prefill / extend kernels, split-KV and extend reductions).
+
+Default workload (the headline): decode-only GQA, 256 requests with context
+U[1024, 8192], 32 query / 4 KV heads, head dim 128, block 16. The metric is
+the decode KV stream rate (algorithmic K+V bytes per step / step time). The
+prefill, mixed and MLA workloads are timed after it and reported under
+"workloads" (they are not the headline number).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 launch with torch.distributed.run: every rank runs its own batch
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_attention_07_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode KV GB/s & tokens/s; prefill/extend TFLOPS; % of HBM / BF16 roofline"
+
+
+# ---------------------------------------------------------------- work model
+def algorithmic_work(spec: W.BatchSpec) -> dict:
+    """Bytes and flops a step must move/do, counted once (no re-reads)."""
+    Hq, Hkv, d, dv = spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.head_dim_v
+    nd, ne = spec.num_decodes, spec.num_extends
+    row_bytes = (d * 2) if spec.mla else Hkv * (d + dv) * 2  # one key's K+V (latent: one row)
+    dec_keys = sum(spec.seq_lens[:nd])
+    dec_bytes = dec_keys * row_bytes
+    dec_flops = dec_keys * Hq * 2 * (d + dv)
+    pair_flops = Hq * 2 * (d + dv)  # per visible (query, key) pair
+    ext_pairs = 0
+    for r in range(nd, nd + ne):
+        q, c = spec.qlen[r], spec.ctx[r]
+        ext_pairs += q * c + q * (q + 1) // 2
+    pre_pairs = sum(q * (q + 1) // 2 for q in spec.qlen[nd + ne:])
+    cw_bytes = 2 * spec.num_tokens * row_bytes  # read + write
+    return {"dec_bytes": dec_bytes, "dec_flops": dec_flops, "ext_flops": ext_pairs * pair_flops,
+            "pre_flops": pre_pairs * pair_flops, "cache_write_bytes": cw_bytes,
+            "tokens": spec.num_tokens, "decode_tokens": nd}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def kernel_traffic(kernel_file: str, key: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        ent = t[key]
+        src = open(os.path.join(ROOT, "paged_kv_attention_07_gb300", "csrc", kernel_file), "rb").read()
+        if hashlib.sha256(src).hexdigest()[:16] != ent["source_sha"]:
+            return None
+        return float(ent["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15] or [p for (_, p) in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+def make_device_batch(spec, device, seed):
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    batch = W.make_batch(spec, values=False)
+    return DeviceBatch(batch, device=device, values_on_device_seed=seed)
+
+
+def time_steps(db, steps, warmup, flush_bytes=0, kernels=(), barrier=None):
+    """Warm up, then time `steps` steps with CUDA events (L2 flushed between
+    steps when flush_bytes > 0). Returns (ms per step, kernel stats, launches)."""
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device=db.device) if flush_bytes else None
+    for _ in range(warmup):
+        db.step()
+    all_k = list(pka.KERNELS)
+    for k in all_k:
+        pka.pka_kernel_timer(k, True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(float(i))
+        ev[i][0].record(stream)
+        db.step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if barrier:
+        barrier()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    stats, launches = {}, 0
+    for k in all_k:
+        tot, n, timed = pka.pka_kernel_timer_read(k)
+        launches += n
+        if timed:
+            stats[k] = {"avg_ms": tot / timed, "launches": n}
+        pka.pka_kernel_timer(k, False)
+    return ms, stats, launches, (t0, t1)
+
+
+def e2e_steps(db, steps, warmup):
+    """Same step through the public API with host-resident inputs: pinned
+    host -> device copies of the step's inputs, the step, and a device -> host
+    read of out and lse, all inside the timed region."""
+    import torch
+    stream = torch.cuda.current_stream()
+    names = ["q", "k_new", "v_new", "slot_mapping", "qsl", "seq_lens", "block_table"]
+    host = {n: getattr(db, n).cpu().pin_memory() for n in names if getattr(db, n) is not None}
+    out_h = torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()
+    lse_h = torch.empty(db.lse.shape, dtype=db.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def one():
+        for n, t in host.items():
+            getattr(db, n).copy_(t, non_blocking=True)
+        db.step()
+        out_h.copy_(db.out, non_blocking=True)
+        lse_h.copy_(db.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def roofline(bound, achieved, peak, unit, traffic):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic}
+
+
+def secondary_workloads(device, steps, warmup, peaks, rank):
+    """Prefill, mixed and MLA workloads, timed one after the other."""
+    import torch
+    res = {}
+    cases = [("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20),
+             ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0),
+             ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0),
+             ("mla_decode_bs1", W.spec_mla_decode(block_size=1), "decode", "hbm", 0)]
+    for name, spec, dom, bound, flush in cases:
+        db = make_device_batch(spec, device, seed=1234 + rank)
+        ms, stats, launches, _ = time_steps(db, steps, warmup, flush_bytes=flush)
+        w = algorithmic_work(spec)
+        ent = {"ms_per_step": round(ms, 4), "tokens_per_s": round(w["tokens"] / (ms * 1e-3), 1),
+               "kernels": {k: round(v["avg_ms"], 4) for k, v in stats.items()}}
+        kms = stats.get(dom, {}).get("avg_ms")
+        if bound == "tensor":
+            flops = w["ext_flops"] + w["pre_flops"]
+            ent["tflops_step"] = round(flops / (ms * 1e-3) / 1e12, 2)
+            if kms:
+                ent["roofline"] = roofline("tensor", flops / (kms * 1e-3) / 1e12, peaks["bf16_tflops"],
+                                           "TFLOP/s", None)
+            if w["dec_bytes"]:
+                dk = stats.get("decode", {}).get("avg_ms")
+                if dk:
+                    ent["decode_kv_gbs"] = round(w["dec_bytes"] / (dk * 1e-3) / 1e9, 1)
+        else:
+            ent["kv_gbs_step"] = round(w["dec_bytes"] / (ms * 1e-3) / 1e9, 1)
+            if kms:
+                ent["roofline"] = roofline("hbm", w["dec_bytes"] / (kms * 1e-3) / 1e9, peaks["hbm_gbs"],
+                                           "GB/s", None)
+                ent["tflops_decode_kernel"] = round(w["dec_flops"] / (kms * 1e-3) / 1e12, 1)
+        res[name] = ent
+        del db
+        torch.cuda.empty_cache()
+    return res
+
+
+class OracleStep:
+    """One step of the oracle on a host batch: cache write of the new tokens
+    into a cache that already holds the context (prepared once, untimed),
+    then float64 attention of every row."""
+
+    def __init__(self, batch):
+        import oracle
+        self.o = oracle
+        self.batch = batch
+        self.kc, self.vc = oracle.populate_cache(batch, "context")
+        self.cores = oracle.default_threads()
+
+    def __call__(self):
+        b, s = self.batch, self.batch.spec
+        self.o.cache_write(b.k_new, b.v_new, b.slot_mapping, self.kc, self.vc, s.block_size)
+        return self.o.attention(b.q, self.kc, self.vc, b.block_table, b.query_start_loc, b.seq_lens,
+                                s.scale, s.block_size, head_dim_v=s.head_dim_v, nthreads=self.cores)
+
+
+def cpu_baseline(spec, max_reqs=64):
+    """The float64 oracle on the host cores, on a bounded sample (the first
+    `max_reqs` requests of the same workload). Returns (GB/s, cores, sample)."""
+    idx = list(range(min(max_reqs, spec.num_reqs)))
+    sub = W.subset(spec, idx)
+    step = OracleStep(W.make_batch(sub))
+    cores = step.cores
+    t0 = time.time()
+    step()
+    dt = time.time() - t0
+    w = algorithmic_work(sub)
+    return w["dec_bytes"] / dt / 1e9, cores, f"{len(idx)} of {spec.num_reqs} requests ({dt:.1f} s)", dt
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    peaks = load_peaks()
+    spec = W.spec_decode_gqa()
+    db = make_device_batch(spec, device, seed=42 + rank)
+    w = algorithmic_work(spec)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ms, stats, launches, (t0, t1) = time_steps(db, args.steps, args.warmup, kernels=("decode",),
+                                               barrier=barrier)
+    # keep the GPU busy long enough for the sampler to see the clocks under load
+    extra_t0 = time.time()
+    while time.time() - extra_t0 < 1.0:
+        db.step()
+    torch.cuda.synchronize()
+    sampler.stop()
+    clocks = sampler.summary(t0, max(t1, extra_t0 + 1.0))
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * w["dec_bytes"] / (ms * 1e-3) / 1e9
+    dec_ms = stats["decode"]["avg_ms"]
+    achieved = w["dec_bytes"] / (dec_ms * 1e-3) / 1e9
+    traffic = kernel_traffic("decode_gqa.cu", "decode_gqa")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random block table)",
+        "config": {"workload": "decode_gqa: 256 decode requests, ctx U[1024,8192], 32 q / 4 kv heads, "
+                               "head_dim 128, block 16", "l2": "inputs larger than L2 (2.4 GB KV)",
+                   "parallelism": f"replicas x{world}"},
+        "decode_tokens_per_s": round(world * w["decode_tokens"] / (ms * 1e-3), 1),
+        "roofline": roofline("hbm", achieved, peaks["hbm_gbs"], "GB/s", traffic),
+        "roofline_peak_source": peaks["source"],
+        "kernels_ms": {k: round(v["avg_ms"], 4) for k, v in stats.items()},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if args.e2e:
+        e_ms, h2d, d2h = e2e_steps(db, max(3, args.steps // 2), 2)
+        line["e2e"] = {"value": round(world * w["dec_bytes"] / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e_ms, 5)}
+    del db
+    torch.cuda.empty_cache()
+    if args.all_workloads:
+        line["workloads"] = secondary_workloads(device, max(3, args.steps // 2), args.warmup, peaks, rank)
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        v, cores, sample, _ = cpu_baseline(spec)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle (float64 C, host cores) as the reference arm, on a bounded
+    sample of the same workload per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    spec = W.spec_decode_gqa()
+    sub = W.subset(spec, list(range(16)))
+    step = OracleStep(W.make_batch(sub))
+    cores = step.cores
+    for _ in range(args.warmup):
+        step()
+    t0 = time.time()
+    for _ in range(args.steps):
+        step()
+    dt = (time.time() - t0) / args.steps
+    wk = algorithmic_work(sub)
+    value = wk["dec_bytes"] / dt / 1e9
+    sample = f"16 of 256 requests per step ({dt:.2f} s per step)"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, random block table)",
+            "config": {"workload": "decode_gqa: 256 decode requests, ctx U[1024,8192], 32 q / 4 kv heads, "
+                                   "head_dim 128, block 16"},
+            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--primary-only", dest="all_workloads", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,532 @@
+// api.cu -- host side of the C ABI (include/pka.h): argument validation,
+// workspace layout, TMA descriptor encoding and the launch sequence of one
+// step. Everything is asynchronous on the caller's stream; nothing here
+// allocates device memory.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "params.cuh"
+#include "plan.cuh"
+
+namespace pka {
+
+// kernels (defined in the other translation units)
+cudaError_t launch_planner(const PlanParams& p, cudaStream_t stream);
+cudaError_t launch_cache_write(const void* k, const void* v, const int64_t* slots, int64_t T, int Hkv,
+                               int d, int dv, void* k_cache, void* v_cache, int64_t num_blocks, int bs,
+                               int32_t* err, int num_sms, cudaStream_t stream);
+cudaError_t launch_merge_pair(void* out, float* out_lse, const void* a, const float* a_lse, const void* b,
+                              const float* b_lse, int64_t rows, int dv, int io_dtype, int num_sms,
+                              cudaStream_t stream);
+
+cudaError_t launch_decode_gqa(const CUtensorMap& km, const CUtensorMap& vm, const DecodeGqaParams& p,
+                              int head_dim, bool tma, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode_mla(const CUtensorMap& map, const DecodeMlaParams& p, bool tma, int num_sms,
+                              cudaStream_t stream);
+cudaError_t launch_fa_fwd(const FaParams& p, int head_dim, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode_reduce(const DecodeReduceParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bound, int num_sms,
+                                 cudaStream_t stream);
+int decode_gqa_target_units(int num_sms);
+int decode_mla_heads_per_cta(int Hq);
+
+namespace {
+
+constexpr int kMlaMinSplit = 1024;
+
+int device_sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D bf16 view [rows, cols] (row-major, dense) read in boxes of
+// 64 columns x box_rows rows with the 128-byte swizzle.
+bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+struct Hints {
+    int nd, ne, np, T, Hq, Hkv, d, dv, maxq, maxs, chunk;
+    bool mla;
+};
+
+// Returns false if the hints are not a shape this build supports.
+bool compute_layout(const Hints& h, int num_sms, Layout* L) {
+    std::memset(L, 0, sizeof(*L));
+    size_t off = sizeof(PlanHeader);
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align256(off + bytes);
+        return o;
+    };
+    const int upp = h.mla ? h.Hq / decode_mla_heads_per_cta(h.Hq) : h.Hkv;
+    L->dec_target_units = h.mla ? num_sms * 4 : decode_gqa_target_units(num_sms);
+    if (L->dec_target_units < 1) L->dec_target_units = 1;
+    const int64_t pair_cap = h.nd > 0 ? (int64_t)L->dec_target_units / upp + h.nd + 1 : 0;
+    int64_t item_cap = 0, row_cap = 0;
+    if (h.ne + h.np > 0) {
+        const int64_t t_nd = (int64_t)h.T - h.nd;
+        const int64_t smax = h.ne > 0 ? 1 + ceil_div(std::max(0, h.maxs - 2), h.chunk) : 1;
+        item_cap = (ceil_div(t_nd, kFaBlockM) + h.ne + h.np) * smax;
+        if (h.ne > 0) row_cap = std::min<int64_t>(t_nd - h.np, (int64_t)h.ne * h.maxq) * smax;
+        if (row_cap < 0) row_cap = 0;
+    }
+    if (pair_cap > INT32_MAX / 4 || item_cap > INT32_MAX / 4 || row_cap > INT32_MAX / 4) return false;
+    L->dec_pair_cap = (int)pair_cap;
+    L->fa_item_cap = (int)item_cap;
+    L->ext_row_cap = (int)row_cap;
+    L->off_dec_pairs = take(sizeof(int2) * (size_t)pair_cap);
+    L->off_dec_first = take(sizeof(int32_t) * (size_t)h.nd);
+    L->off_dec_nsplit = take(sizeof(int32_t) * (size_t)h.nd);
+    L->off_fa_items = take(sizeof(int4) * (size_t)item_cap);
+    L->off_ext_base = take(sizeof(int32_t) * (size_t)h.ne);
+    L->off_dec_part_o = take(sizeof(float) * (size_t)pair_cap * h.Hq * h.dv);
+    L->off_dec_part_lse = take(sizeof(float) * (size_t)pair_cap * h.Hq);
+    L->off_ext_part_o = take(sizeof(float) * (size_t)row_cap * h.Hq * h.dv);
+    L->off_ext_part_lse = take(sizeof(float) * (size_t)row_cap * h.Hq);
+    L->total = off;
+    return true;
+}
+
+pka_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA; }
+
+// ---- kernel timers (benchmarking aid)
+constexpr int kTimerSlots = 4096;
+struct KernelTimer {
+    bool on = false;
+    int launches = 0;
+    int timed = 0;
+    cudaEvent_t ev[2 * kTimerSlots] = {};
+};
+KernelTimer g_timers[PKA_KERNEL_COUNT];
+std::mutex g_timer_mu;
+
+// Records the start event of a timed launch; returns the slot or -1.
+int timer_begin(int kernel, cudaStream_t st) {
+    KernelTimer& t = g_timers[kernel];
+    if (!t.on) return -1;
+    std::lock_guard<std::mutex> lock(g_timer_mu);
+    ++t.launches;
+    if (t.timed >= kTimerSlots) return -1;
+    const int slot = t.timed;
+    for (int i = 0; i < 2; ++i)
+        if (!t.ev[2 * slot + i] && cudaEventCreate(&t.ev[2 * slot + i]) != cudaSuccess) return -1;
+    if (cudaEventRecord(t.ev[2 * slot], st) != cudaSuccess) return -1;
+    return slot;
+}
+
+void timer_end(int kernel, int slot, cudaStream_t st) {
+    if (slot < 0) return;
+    KernelTimer& t = g_timers[kernel];
+    std::lock_guard<std::mutex> lock(g_timer_mu);
+    if (cudaEventRecord(t.ev[2 * slot + 1], st) == cudaSuccess) t.timed = slot + 1;
+}
+
+// Runs `launch` bracketed by the timer of `kernel` (when enabled).
+template <typename F>
+cudaError_t timed(int kernel, cudaStream_t st, F&& launch) {
+    const int slot = timer_begin(kernel, st);
+    const cudaError_t e = launch();
+    timer_end(kernel, slot, st);
+    return e;
+}
+
+}  // namespace
+}  // namespace pka
+
+using namespace pka;
+
+extern "C" {
+
+const char* pka_status_string(pka_status s) {
+    switch (s) {
+        case PKA_OK: return "ok";
+        case PKA_ERR_INVALID_ARG: return "invalid argument";
+        case PKA_ERR_UNSUPPORTED: return "unsupported shape";
+        case PKA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case PKA_ERR_CUDA: return "CUDA error";
+        case PKA_ERR_DEVICE_METADATA: return "device metadata error";
+    }
+    return "unknown status";
+}
+
+pka_status pka_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                           int num_kv_heads, int head_dim, int head_dim_v, void* k_cache, void* v_cache,
+                           int64_t num_blocks, int block_size, int32_t* error_word, void* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
+        return PKA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKA_OK;
+    if (!k || !slot_mapping || !k_cache) return PKA_ERR_INVALID_ARG;
+    if ((v == nullptr) != (v_cache == nullptr)) return PKA_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0 || (v && (head_dim_v <= 0 || head_dim_v % 8 != 0))) return PKA_ERR_UNSUPPORTED;
+    if (!aligned(k, 16) || !aligned(k_cache, 16) || (v && (!aligned(v, 16) || !aligned(v_cache, 16))) ||
+        !aligned(slot_mapping, 8))
+        return PKA_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return PKA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(timed(PKA_KERNEL_CACHE_WRITE, st, [&] {
+        return launch_cache_write(k, v, slot_mapping, num_tokens, num_kv_heads, head_dim, head_dim_v, k_cache,
+                                  v_cache, num_blocks, block_size, error_word, sms, st);
+    }));
+}
+
+static pka_status check_shape(int nd, int ne, int np, int T, int Hq, int Hkv, int d, int dv, int maxq,
+                              int maxs, int chunk, bool mla, bool* is_mla) {
+    if (nd < 0 || ne < 0 || np < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || maxq <= 0 || maxs <= 0)
+        return PKA_ERR_INVALID_ARG;
+    const int B = nd + ne + np;
+    if (B > kMaxRequests) return PKA_ERR_UNSUPPORTED;
+    if ((int64_t)T < (int64_t)nd + 2LL * ne + np) return PKA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return PKA_ERR_INVALID_ARG;
+    if (maxs < maxq) return PKA_ERR_INVALID_ARG;
+    if (chunk < 16) return PKA_ERR_INVALID_ARG;
+    if (mla) {
+        if (!(d == 576 && dv == 512 && Hkv == 1)) return PKA_ERR_UNSUPPORTED;
+        if (!(Hq == 16 || Hq == 32 || Hq % 64 == 0)) return PKA_ERR_UNSUPPORTED;
+        if (ne + np > 0) return PKA_ERR_UNSUPPORTED;
+    } else {
+        if (!((d == 64 || d == 128) && dv == d)) return PKA_ERR_UNSUPPORTED;
+        if (Hq / Hkv > 16) return PKA_ERR_UNSUPPORTED;
+    }
+    *is_mla = mla;
+    return PKA_OK;
+}
+
+size_t pka_workspace_size(int num_decodes, int num_extends, int num_prefills, int num_tokens, int num_q_heads,
+                          int num_kv_heads, int head_dim, int head_dim_v, int max_query_len, int max_seq_len,
+                          int context_chunk_tokens) {
+    const bool mla = head_dim == 576;
+    bool is_mla = false;
+    if (check_shape(num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads, head_dim,
+                    head_dim_v, max_query_len, max_seq_len, context_chunk_tokens, mla, &is_mla) != PKA_OK)
+        return 0;
+    const int sms = device_sm_count();
+    if (sms <= 0) return 0;
+    Hints h{num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads, head_dim,
+            head_dim_v, max_query_len, max_seq_len, context_chunk_tokens, is_mla};
+    Layout L;
+    if (!compute_layout(h, sms, &L)) return 0;
+    return L.total;
+}
+
+pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table, int max_blocks_per_req,
+                                  const int32_t* query_start_loc, const int32_t* seq_lens, int num_decodes,
+                                  int num_extends, int num_prefills, int num_tokens, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int head_dim_v, int64_t num_blocks,
+                                  int block_size, float scale, int context_chunk_tokens, int max_query_len,
+                                  int max_seq_len, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int B = num_decodes + num_extends + num_prefills;
+    if (B == 0 && num_tokens == 0) return PKA_OK;
+    // ---- host validation: nothing is launched on failure
+    const bool mla = v_cache == nullptr;
+    bool is_mla = false;
+    pka_status sc = check_shape(num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads,
+                                head_dim, head_dim_v, max_query_len, max_seq_len, context_chunk_tokens, mla,
+                                &is_mla);
+    if (sc != PKA_OK) return sc;
+    if (B < 1) return PKA_ERR_INVALID_ARG;
+    if (!q || !k_cache || !block_table || !query_start_loc || !seq_lens || !out || !workspace)
+        return PKA_ERR_INVALID_ARG;
+    if (num_extends + num_prefills > 0 && (!k_new || !v_new)) return PKA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || (v_cache && !aligned(v_cache, 16)) || !aligned(out, 16) ||
+        !aligned(workspace, 256) || (k_new && !aligned(k_new, 16)) || (v_new && !aligned(v_new, 16)) ||
+        (lse && !aligned(lse, 4)))
+        return PKA_ERR_INVALID_ARG;
+    if (max_blocks_per_req <= 0 || num_blocks <= 0 || !pow2(block_size) || block_size > 128)
+        return block_size > 128 || !pow2(block_size) ? PKA_ERR_UNSUPPORTED : PKA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKA_ERR_INVALID_ARG;
+    const int64_t cache_rows = num_blocks * num_kv_heads * (int64_t)block_size;
+    if (cache_rows >= (int64_t)INT32_MAX) return PKA_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_req * block_size < max_seq_len) return PKA_ERR_INVALID_ARG;
+
+    const int sms = device_sm_count();
+    if (sms <= 0) return PKA_ERR_CUDA;
+    Hints h{num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads, head_dim, head_dim_v,
+            max_query_len, max_seq_len, context_chunk_tokens, is_mla};
+    Layout L;
+    if (!compute_layout(h, sms, &L)) return PKA_ERR_UNSUPPORTED;
+    if (workspace_bytes < L.total) return PKA_ERR_WORKSPACE_TOO_SMALL;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
+    cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(PlanHeader), st);
+    if (e != cudaSuccess) return PKA_ERR_CUDA;
+
+    // ---- plan
+    PlanParams pp;
+    pp.qsl = query_start_loc;
+    pp.seq_lens = seq_lens;
+    pp.num_decodes = num_decodes;
+    pp.num_extends = num_extends;
+    pp.num_prefills = num_prefills;
+    pp.num_tokens = num_tokens;
+    pp.max_query_len = max_query_len;
+    pp.max_seq_len = max_seq_len;
+    pp.max_blocks_per_req = max_blocks_per_req;
+    pp.block_size = block_size;
+    pp.chunk = context_chunk_tokens;
+    pp.dec_units_per_pair = is_mla ? num_q_heads / decode_mla_heads_per_cta(num_q_heads) : num_kv_heads;
+    pp.dec_target_units = L.dec_target_units;
+    pp.dec_min_split = is_mla ? kMlaMinSplit : kDecodeMinSplit;
+    pp.dec_pair_cap = L.dec_pair_cap;
+    pp.fa_item_cap = L.fa_item_cap;
+    pp.ext_row_cap = L.ext_row_cap;
+    pp.hdr = hdr;
+    pp.dec_pairs = reinterpret_cast<int2*>(ws + L.off_dec_pairs);
+    pp.dec_first = reinterpret_cast<int32_t*>(ws + L.off_dec_first);
+    pp.dec_nsplit = reinterpret_cast<int32_t*>(ws + L.off_dec_nsplit);
+    pp.fa_items = reinterpret_cast<int4*>(ws + L.off_fa_items);
+    pp.ext_base = reinterpret_cast<int32_t*>(ws + L.off_ext_base);
+    if ((e = timed(PKA_KERNEL_PLANNER, st, [&] { return launch_planner(pp, st); })) != cudaSuccess)
+        return PKA_ERR_CUDA;
+
+    const float scale_log2 = scale * 1.4426950408889634f;
+    auto* outb = static_cast<__nv_bfloat16*>(out);
+    float* dec_po = reinterpret_cast<float*>(ws + L.off_dec_part_o);
+    float* dec_pl = reinterpret_cast<float*>(ws + L.off_dec_part_lse);
+
+    // ---- decode slice
+    if (num_decodes > 0) {
+        const bool tma = block_size >= 8;
+        if (is_mla) {
+            CUtensorMap map;
+            std::memset(&map, 0, sizeof(map));
+            if (tma && !encode_rows(&map, k_cache, (uint64_t)cache_rows, 576, (uint32_t)std::min(block_size, 16)))
+                return PKA_ERR_CUDA;
+            DecodeMlaParams dp;
+            dp.q = static_cast<const __nv_bfloat16*>(q);
+            dp.kv = static_cast<const __nv_bfloat16*>(k_cache);
+            dp.block_table = block_table;
+            dp.seq_lens = seq_lens;
+            dp.hdr = hdr;
+            dp.counter = &hdr->dec_counter;
+            dp.err = &hdr->err;
+            dp.pairs = pp.dec_pairs;
+            dp.nsplit = pp.dec_nsplit;
+            dp.part_o = dec_po;
+            dp.part_lse = dec_pl;
+            dp.out = outb;
+            dp.lse = lse;
+            dp.num_blocks = num_blocks;
+            dp.max_blocks = max_blocks_per_req;
+            dp.Hq = num_q_heads;
+            dp.bs = block_size;
+            dp.groups = num_q_heads / decode_mla_heads_per_cta(num_q_heads);
+            dp.scale_log2 = scale_log2;
+            if ((e = timed(PKA_KERNEL_DECODE, st, [&] { return launch_decode_mla(map, dp, tma, sms, st); })) !=
+                cudaSuccess)
+                return PKA_ERR_CUDA;
+        } else {
+            CUtensorMap km, vm;
+            std::memset(&km, 0, sizeof(km));
+            std::memset(&vm, 0, sizeof(vm));
+            if (tma) {
+                const uint32_t br = (uint32_t)std::min(block_size, 16);
+                if (!encode_rows(&km, k_cache, (uint64_t)cache_rows, head_dim, br) ||
+                    !encode_rows(&vm, v_cache, (uint64_t)cache_rows, head_dim, br))
+                    return PKA_ERR_CUDA;
+            }
+            DecodeGqaParams dp;
+            dp.q = static_cast<const __nv_bfloat16*>(q);
+            dp.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+            dp.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+            dp.block_table = block_table;
+            dp.seq_lens = seq_lens;
+            dp.hdr = hdr;
+            dp.counter = &hdr->dec_counter;
+            dp.err = &hdr->err;
+            dp.pairs = pp.dec_pairs;
+            dp.nsplit = pp.dec_nsplit;
+            dp.part_o = dec_po;
+            dp.part_lse = dec_pl;
+            dp.out = outb;
+            dp.lse = lse;
+            dp.num_blocks = num_blocks;
+            dp.max_blocks = max_blocks_per_req;
+            dp.Hq = num_q_heads;
+            dp.Hkv = num_kv_heads;
+            dp.G = num_q_heads / num_kv_heads;
+            dp.bs = block_size;
+            dp.scale_log2 = scale_log2;
+            if ((e = timed(PKA_KERNEL_DECODE, st,
+                           [&] { return launch_decode_gqa(km, vm, dp, head_dim, tma, sms, st); })) != cudaSuccess)
+                return PKA_ERR_CUDA;
+        }
+        DecodeReduceParams rp;
+        rp.hdr = hdr;
+        rp.dec_first = pp.dec_first;
+        rp.dec_nsplit = pp.dec_nsplit;
+        rp.part_o = dec_po;
+        rp.part_lse = dec_pl;
+        rp.out = outb;
+        rp.lse = lse;
+        rp.num_decodes = num_decodes;
+        rp.Hq = num_q_heads;
+        rp.dv = head_dim_v;
+        if ((e = timed(PKA_KERNEL_DECODE_REDUCE, st, [&] { return launch_decode_reduce(rp, sms, st); })) !=
+            cudaSuccess)
+            return PKA_ERR_CUDA;
+    }
+
+    // ---- prefill + extend slices
+    if (num_extends + num_prefills > 0) {
+        FaParams fp;
+        fp.q = static_cast<const __nv_bfloat16*>(q);
+        fp.k_new = static_cast<const __nv_bfloat16*>(k_new);
+        fp.v_new = static_cast<const __nv_bfloat16*>(v_new);
+        fp.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+        fp.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+        fp.block_table = block_table;
+        fp.qsl = query_start_loc;
+        fp.seq_lens = seq_lens;
+        fp.hdr = hdr;
+        fp.counter = &hdr->fa_counter;
+        fp.err = &hdr->err;
+        fp.items = pp.fa_items;
+        fp.ext_base = pp.ext_base;
+        fp.ext_o = reinterpret_cast<float*>(ws + L.off_ext_part_o);
+        fp.ext_lse = reinterpret_cast<float*>(ws + L.off_ext_part_lse);
+        fp.out = outb;
+        fp.lse = lse;
+        fp.num_blocks = num_blocks;
+        fp.max_blocks = max_blocks_per_req;
+        fp.Hq = num_q_heads;
+        fp.Hkv = num_kv_heads;
+        fp.G = num_q_heads / num_kv_heads;
+        fp.bs = block_size;
+        fp.chunk = context_chunk_tokens;
+        fp.num_decodes = num_decodes;
+        fp.num_extends = num_extends;
+        fp.scale_log2 = scale_log2;
+        if ((e = timed(PKA_KERNEL_PREFILL_EXTEND, st, [&] { return launch_fa_fwd(fp, head_dim, sms, st); })) !=
+            cudaSuccess)
+            return PKA_ERR_CUDA;
+        if (num_extends > 0) {
+            ExtendReduceParams xp;
+            xp.hdr = hdr;
+            xp.qsl = query_start_loc;
+            xp.seq_lens = seq_lens;
+            xp.ext_base = pp.ext_base;
+            xp.part_o = fp.ext_o;
+            xp.part_lse = fp.ext_lse;
+            xp.out = outb;
+            xp.lse = lse;
+            xp.num_decodes = num_decodes;
+            xp.num_extends = num_extends;
+            xp.Hq = num_q_heads;
+            xp.dv = head_dim_v;
+            xp.chunk = context_chunk_tokens;
+            const int ext_tokens_bound = std::min(num_tokens - num_decodes - num_prefills,
+                                                  num_extends * max_query_len);
+            if ((e = timed(PKA_KERNEL_EXTEND_REDUCE, st,
+                           [&] { return launch_extend_reduce(xp, ext_tokens_bound, sms, st); })) != cudaSuccess)
+                return PKA_ERR_CUDA;
+        }
+    }
+    return PKA_OK;
+}
+
+pka_status pka_merge_attn_states(void* out, float* out_lse, const void* prefix_out, const float* prefix_lse,
+                                 const void* suffix_out, const float* suffix_lse, int64_t num_rows, int head_dim,
+                                 int io_dtype, void* stream) {
+    if (num_rows < 0 || head_dim <= 0 || (io_dtype != 0 && io_dtype != 1)) return PKA_ERR_INVALID_ARG;
+    if (num_rows == 0) return PKA_OK;
+    if (!out || !prefix_out || !prefix_lse || !suffix_out || !suffix_lse) return PKA_ERR_INVALID_ARG;
+    if (head_dim % (io_dtype ? 8 : 4) != 0) return PKA_ERR_UNSUPPORTED;
+    if (!aligned(out, 16) || !aligned(prefix_out, 16) || !aligned(suffix_out, 16) || !aligned(prefix_lse, 4) ||
+        !aligned(suffix_lse, 4) || (out_lse && !aligned(out_lse, 4)))
+        return PKA_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return PKA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(timed(PKA_KERNEL_MERGE, st, [&] {
+        return launch_merge_pair(out, out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse, num_rows, head_dim,
+                                 io_dtype, sms, st);
+    }));
+}
+
+pka_status pka_kernel_timer(int kernel, int enable) {
+    if (kernel < 0 || kernel >= PKA_KERNEL_COUNT) return PKA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_timer_mu);
+    KernelTimer& t = g_timers[kernel];
+    t.on = enable != 0;
+    t.launches = 0;
+    t.timed = 0;
+    return PKA_OK;
+}
+
+pka_status pka_kernel_timer_read(int kernel, double* total_ms, int* launches, int* timed_out) {
+    if (kernel < 0 || kernel >= PKA_KERNEL_COUNT) return PKA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_timer_mu);
+    KernelTimer& t = g_timers[kernel];
+    double sum = 0.0;
+    for (int i = 0; i < t.timed; ++i) {
+        if (cudaEventSynchronize(t.ev[2 * i + 1]) != cudaSuccess) return PKA_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess) return PKA_ERR_CUDA;
+        sum += ms;
+    }
+    if (total_ms) *total_ms = sum;
+    if (launches) *launches = t.launches;
+    if (timed_out) *timed_out = t.timed;
+    return PKA_OK;
+}
+
+pka_status pka_get_error(const void* workspace, int32_t* code_out, void* stream) {
+    if (!workspace) return PKA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t code = 0;
+    if (cudaMemcpyAsync(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return PKA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PKA_ERR_CUDA;
+    if (code_out) *code_out = code;
+    return code ? PKA_ERR_DEVICE_METADATA : PKA_OK;
+}
+
+}  // extern "C"

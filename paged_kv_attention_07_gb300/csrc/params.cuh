@@ -1,0 +1,97 @@
+// params.cuh -- launch parameter blocks of the attention kernels, shared by
+// the kernels and the host code that fills them (api.cu).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "plan.cuh"
+
+namespace pka {
+
+struct DecodeGqaParams {
+    const __nv_bfloat16* q;        // [T, Hq, D]
+    const __nv_bfloat16* k_cache;  // [nb, Hkv, bs, D]
+    const __nv_bfloat16* v_cache;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const PlanHeader* hdr;
+    int32_t* counter;
+    int32_t* err;
+    const int2* pairs;
+    const int32_t* nsplit;
+    float* part_o;
+    float* part_lse;
+    __nv_bfloat16* out;
+    float* lse;
+    int64_t num_blocks;
+    int max_blocks, Hq, Hkv, G, bs;
+    float scale_log2;
+};
+
+struct DecodeMlaParams {
+    const __nv_bfloat16* q;   // [T, Hq, 576]
+    const __nv_bfloat16* kv;  // [nb, bs, 576]
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const PlanHeader* hdr;
+    int32_t* counter;
+    int32_t* err;
+    const int2* pairs;
+    const int32_t* nsplit;
+    float* part_o;
+    float* part_lse;
+    __nv_bfloat16* out;
+    float* lse;
+    int64_t num_blocks;
+    int max_blocks, Hq, bs, groups;  // groups = Hq / (8 * NW)
+    float scale_log2;
+};
+
+struct FaParams {
+    const __nv_bfloat16* q;      // [T, Hq, D]
+    const __nv_bfloat16* k_new;  // [T, Hkv, D]
+    const __nv_bfloat16* v_new;
+    const __nv_bfloat16* k_cache;  // [nb, Hkv, bs, D]
+    const __nv_bfloat16* v_cache;
+    const int32_t* block_table;
+    const int32_t* qsl;
+    const int32_t* seq_lens;
+    const PlanHeader* hdr;
+    int32_t* counter;
+    int32_t* err;
+    const int4* items;
+    const int32_t* ext_base;
+    float* ext_o;
+    float* ext_lse;
+    __nv_bfloat16* out;
+    float* lse;
+    int64_t num_blocks;
+    int max_blocks, Hq, Hkv, G, bs, chunk, num_decodes, num_extends;
+    float scale_log2;
+};
+
+struct DecodeReduceParams {
+    const PlanHeader* hdr;
+    const int32_t* dec_first;
+    const int32_t* dec_nsplit;
+    const float* part_o;
+    const float* part_lse;
+    __nv_bfloat16* out;
+    float* lse;
+    int num_decodes, Hq, dv;
+};
+
+struct ExtendReduceParams {
+    const PlanHeader* hdr;
+    const int32_t* qsl;
+    const int32_t* seq_lens;
+    const int32_t* ext_base;
+    const float* part_o;
+    const float* part_lse;
+    __nv_bfloat16* out;
+    float* lse;
+    int num_decodes, num_extends, Hq, dv, chunk;
+};
+
+}  // namespace pka

@@ -1,0 +1,91 @@
+"""A synthetic batch resident on the GPU, driven through the C ABI.
+
+Holds the device copies of a `workloads.Batch` (metadata, Q, the new
+tokens' K/V, the paged caches, outputs and the workspace) and runs one step:
+`pka_cache_write` of the new tokens, then `pka_paged_attn_forward`. The
+caches start NaN-poisoned and receive the context rows through
+`pka_cache_write`, so every slot the batch does not own stays NaN.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import pka
+from . import workloads as W
+
+
+def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+class DeviceBatch:
+    def __init__(self, batch: W.Batch, device="cuda", values_on_device_seed: int | None = None):
+        spec = batch.spec
+        self.batch, self.spec, self.device = batch, spec, device
+        Hq, Hkv, d, dv, bs = (spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.head_dim_v,
+                              spec.block_size)
+        T = spec.num_tokens
+        S = int(batch.seq_start[-1])
+        self.qsl = torch.from_numpy(batch.query_start_loc).to(device)
+        self.seq_lens = torch.from_numpy(batch.seq_lens).to(device)
+        self.block_table = torch.from_numpy(batch.block_table).to(device)
+        self.slot_mapping = torch.from_numpy(np.ascontiguousarray(batch.slot_mapping)).to(device)
+        nb = batch.num_blocks
+        self.k_cache = torch.full((nb, Hkv, bs, d), float("nan"), dtype=torch.bfloat16, device=device)
+        self.v_cache = None if spec.mla else torch.full((nb, Hkv, bs, dv), float("nan"),
+                                                        dtype=torch.bfloat16, device=device)
+        if values_on_device_seed is None:
+            self.q = bf16_tensor(batch.q, device)
+            k_seq = bf16_tensor(batch.k_seq, device)
+            v_seq = None if batch.v_seq is None else bf16_tensor(batch.v_seq, device)
+        else:  # same shapes, N(0,1) drawn on the device (fast path for large benchmarks)
+            g = torch.Generator(device=device)
+            g.manual_seed(values_on_device_seed)
+            self.q = torch.randn((T, Hq, d), generator=g, device=device).to(torch.bfloat16)
+            k_seq = torch.randn((S, Hkv, d), generator=g, device=device).to(torch.bfloat16)
+            v_seq = None if spec.mla else torch.randn((S, Hkv, dv), generator=g,
+                                                      device=device).to(torch.bfloat16)
+        new_idx = torch.from_numpy(batch.new_index).to(device)
+        ctx_idx = torch.from_numpy(batch.ctx_index).to(device)
+        slot_all = torch.from_numpy(batch.slot_all).to(device)
+        self.k_new = k_seq.index_select(0, new_idx).contiguous()
+        self.v_new = None if v_seq is None else v_seq.index_select(0, new_idx).contiguous()
+        if ctx_idx.numel():
+            kc = k_seq.index_select(0, ctx_idx).contiguous()
+            vc = None if v_seq is None else v_seq.index_select(0, ctx_idx).contiguous()
+            pka.pka_cache_write(kc, vc, slot_all.index_select(0, ctx_idx).contiguous(),
+                                self.k_cache, self.v_cache)
+            del kc, vc
+        del k_seq, v_seq
+        self.out = torch.zeros((T, Hq, dv), dtype=torch.bfloat16, device=device)
+        self.lse = torch.zeros((T, Hq), dtype=torch.float32, device=device)
+        self.max_query_len = int(max(spec.qlen))
+        self.max_seq_len = int(max(spec.seq_lens))
+        ws = pka.pka_workspace_size(spec.num_decodes, spec.num_extends, spec.num_prefills, T, Hq, Hkv,
+                                    d, dv, self.max_query_len, self.max_seq_len, spec.context_chunk)
+        if ws == 0:
+            raise RuntimeError("pka_workspace_size rejected the batch shape")
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+
+    def cache_write(self, stream=None):
+        pka.pka_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                            stream=stream)
+
+    def forward(self, stream=None, out=None, lse=None):
+        s = self.spec
+        pka.pka_paged_attn_forward(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                   self.block_table, self.qsl, self.seq_lens, s.num_decodes,
+                                   s.num_extends, s.num_prefills, s.scale, s.context_chunk,
+                                   self.max_query_len, self.max_seq_len,
+                                   self.out if out is None else out,
+                                   self.lse if lse is None else lse, self.workspace,
+                                   head_dim_v=s.head_dim_v, stream=stream)
+
+    def step(self, stream=None):
+        self.cache_write(stream)
+        self.forward(stream)
+
+    def error_word(self) -> int:
+        return pka.pka_get_error(self.workspace)

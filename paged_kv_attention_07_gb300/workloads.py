@@ -111,7 +111,7 @@ class Batch:
 
     @property
     def k_new(self) -> np.ndarray:
-        return self.k_seq[self.new_index]
+        return None if self.k_seq is None else self.k_seq[self.new_index]
 
     @property
     def v_new(self) -> np.ndarray | None:
@@ -127,9 +127,11 @@ class Batch:
 
 
 def make_batch(spec: BatchSpec, rng: np.random.Generator | None = None,
-               block_perm: np.ndarray | None = None) -> Batch:
+               block_perm: np.ndarray | None = None, values: bool = True) -> Batch:
     """Materialise a spec: Q, K, V draws, then the block permutation (in that
-    order, so the values do not depend on the block size)."""
+    order, so the values do not depend on the block size). With
+    values=False only the metadata is built (q/k_seq/v_seq are None) and the
+    permutation comes from default_rng(seed + 2000)."""
     if rng is None:
         rng = np.random.default_rng(spec.seed + 1000)
     B = spec.num_reqs
@@ -141,9 +143,13 @@ def make_batch(spec: BatchSpec, rng: np.random.Generator | None = None,
     T = int(ql.sum())
     S = int(seq.sum())
     Hq, Hkv, d, dv = spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.head_dim_v
-    q = _normal_bf16(rng, (T, Hq, d))
-    k_seq = _normal_bf16(rng, (S, Hkv, d))
-    v_seq = None if spec.mla else _normal_bf16(rng, (S, Hkv, dv))
+    if values:
+        q = _normal_bf16(rng, (T, Hq, d))
+        k_seq = _normal_bf16(rng, (S, Hkv, d))
+        v_seq = None if spec.mla else _normal_bf16(rng, (S, Hkv, dv))
+    else:
+        q = k_seq = v_seq = None
+        rng = np.random.default_rng(spec.seed + 2000)
 
     nblk = (seq + bs - 1) // bs
     need = int(nblk.sum())

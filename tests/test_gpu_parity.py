@@ -1,0 +1,240 @@
+"""GPU parity: every path of the CUDA library against the float64 oracle, on
+seeded inputs that span several tiles, ragged tails and the degenerate cases
+(context 0, a single key, block size 1, one query head per kv head)."""
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_attention_07_gb300 import workloads as W
+from tests.gpu_util import LSE_ATOL, OUT_ATOL, check_batch, compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _dec(name, ctx, Hq, Hkv, d, bs, seed, mla=False, dv=None):
+    return W.spec_custom(name, ctx=ctx, qlen=[1] * len(ctx), num_decodes=len(ctx), num_extends=0,
+                         num_prefills=0, Hq=Hq, Hkv=Hkv, d=d, dv=dv or d, bs=bs, mla=mla, seed=seed,
+                         scale=None if not mla else 1 / np.sqrt(192))
+
+
+DEC_CTX = [0, 1, 15, 16, 17, 255, 256, 257, 600, 1500, 4100]
+
+
+def test_tiny_mixed_config():
+    check_batch(W.make_batch(W.spec_tiny()))
+
+
+@pytest.mark.parametrize("bs", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_decode_gqa_block_sizes(bs):
+    check_batch(W.make_batch(_dec(f"dec_bs{bs}", DEC_CTX, 32, 4, 128, bs, seed=bs)))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (32, 4), (32, 2), (6, 3)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_gqa_groups(Hq, Hkv, d):
+    check_batch(W.make_batch(_dec(f"dec_g{Hq // Hkv}", DEC_CTX, Hq, Hkv, d, 16, seed=Hq + d)))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 8])
+def test_prefill_varlen(d, G):
+    lens = [1, 2, 63, 64, 65, 130, 300]
+    spec = W.spec_custom("pre", ctx=[0] * len(lens), qlen=lens, num_decodes=0, num_extends=0,
+                         num_prefills=len(lens), Hq=2 * G, Hkv=2, d=d, dv=d, bs=16, seed=d + G)
+    check_batch(W.make_batch(spec))
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 1000])
+@pytest.mark.parametrize("bs", [1, 16, 64])
+def test_extend_chunks(chunk, bs):
+    spec = W.spec_custom("ext", ctx=[1, 5, 100, 300], qlen=[2, 17, 64, 129], num_decodes=0,
+                         num_extends=4, num_prefills=0, Hq=8, Hkv=2, d=128, dv=128, bs=bs, chunk=chunk,
+                         seed=chunk + bs)
+    check_batch(W.make_batch(spec))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_mixed_three_paths(d):
+    spec = W.spec_custom("mixed_small", ctx=[3, 700, 40, 2000, 0, 0], qlen=[1, 1, 33, 70, 100, 7],
+                         num_decodes=2, num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=d, dv=d, bs=16,
+                         chunk=512, seed=d)
+    check_batch(W.make_batch(spec))
+
+
+@pytest.mark.parametrize("Hq", [16, 32, 64, 128])
+@pytest.mark.parametrize("bs", [1, 4, 16, 64])
+def test_decode_mla(Hq, bs):
+    ctx = [0, 1, 17, 200, 1500, 3000] if Hq == 128 else [0, 17, 1500]
+    spec = _dec("mla", ctx, Hq, 1, 576, bs, seed=Hq + bs, mla=True, dv=512)
+    check_batch(W.make_batch(spec))
+
+
+def test_constant_v_gives_constant_output():
+    spec = W.spec_custom("const", ctx=[0, 90, 30, 0], qlen=[1, 1, 20, 50], num_decodes=2,
+                         num_extends=1, num_prefills=1, Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=32)
+    batch = W.make_batch(spec)
+    batch.v_seq[:] = W.to_bf16_bits(np.array([0.375], np.float32))[0]
+    out, lse, err, _ = run_gpu(batch)
+    assert err == 0
+    assert np.all(out == 0.375)
+
+
+def test_cache_write_bit_exact():
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    from paged_kv_attention_07_gb300.device_batch import bf16_tensor
+    spec = W.spec_custom("cw", ctx=[37, 100, 64, 0], qlen=[1, 1, 16, 48], num_decodes=2, num_extends=1,
+                         num_prefills=1, Hq=4, Hkv=2, d=64, dv=64, bs=16, num_blocks=64, seed=9)
+    batch = W.make_batch(spec)
+    kc_ref, vc_ref = oracle.populate_cache(batch, "context")
+    slots = batch.slot_mapping.copy()
+    slots[5] = -1  # padding token
+    oracle.cache_write(batch.k_new, batch.v_new, slots, kc_ref, vc_ref, spec.block_size)
+    kc = bf16_tensor(oracle.populate_cache(batch, "context")[0], "cuda")
+    vc = bf16_tensor(oracle.populate_cache(batch, "context")[1], "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pka.pka_cache_write(bf16_tensor(batch.k_new, "cuda"), bf16_tensor(batch.v_new, "cuda"),
+                        torch.from_numpy(slots).cuda(), kc, vc, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(kc.view(torch.int16).cpu().numpy().view(np.uint16), kc_ref)
+    assert np.array_equal(vc.view(torch.int16).cpu().numpy().view(np.uint16), vc_ref)
+
+
+def test_cache_write_latent_and_bad_slot():
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    from paged_kv_attention_07_gb300.device_batch import bf16_tensor
+    spec = _dec("cwl", [5, 70], 16, 1, 576, 4, seed=3, mla=True, dv=512)
+    batch = W.make_batch(spec)
+    kc_ref, _ = oracle.populate_cache(batch, "context")
+    slots = batch.slot_mapping.copy()
+    oracle.cache_write(batch.k_new, None, slots, kc_ref, None, spec.block_size)
+    kc = bf16_tensor(oracle.populate_cache(batch, "context")[0], "cuda")
+    bad = slots.copy()
+    bad[0] = kc_ref.shape[0] * spec.block_size + 3  # beyond the cache: skipped + flagged
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pka.pka_cache_write(bf16_tensor(batch.k_new, "cuda"), None, torch.from_numpy(bad).cuda(), kc, None,
+                        error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pka.DEVERR["SLOT"]
+    got = kc.view(torch.int16).cpu().numpy().view(np.uint16)
+    # the good token landed, the bad one was dropped
+    blk, off = divmod(int(slots[1]), spec.block_size)
+    assert np.array_equal(got[blk, 0, off], kc_ref[blk, 0, off])
+    blk0, off0 = divmod(int(slots[0]), spec.block_size)
+    assert np.all(got[blk0, 0, off0] == 0x7FC0)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_merge_attn_states(io):
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    rng = np.random.default_rng(1)
+    n, dv = 777, 128
+    a = rng.standard_normal((n, dv)).astype(np.float32)
+    b = rng.standard_normal((n, dv)).astype(np.float32)
+    la = (rng.standard_normal(n) * 3).astype(np.float32)
+    lb = (rng.standard_normal(n) * 3).astype(np.float32)
+    la[:5] = -np.inf  # empty prefix
+    lb[5:10] = -np.inf  # empty suffix
+    la[10:12] = lb[10:12] = -np.inf  # both empty
+    if io == "bf16":
+        a = W.bf16_bits_to_f32(W.to_bf16_bits(a))
+        b = W.bf16_bits_to_f32(W.to_bf16_bits(b))
+    ref_o, ref_l = oracle.merge_attn_states(a, la, b, lb)
+    dt = torch.float32 if io == "f32" else torch.bfloat16
+    ta, tb = torch.from_numpy(a).cuda().to(dt), torch.from_numpy(b).cuda().to(dt)
+    out = torch.empty_like(ta)
+    out_lse = torch.empty(n, dtype=torch.float32, device="cuda")
+    pka.pka_merge_attn_states(out, out_lse, ta, torch.from_numpy(la).cuda(), tb, torch.from_numpy(lb).cuda())
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    l = out_lse.cpu().numpy()
+    tol = 1e-5 if io == "f32" else OUT_ATOL
+    np.testing.assert_allclose(o, ref_o, atol=tol, rtol=0)
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(l), fin)
+    np.testing.assert_allclose(l[fin], ref_l[fin], atol=1e-5, rtol=0)
+
+
+def test_repeat_is_bitwise_deterministic():
+    import torch
+    spec = W.spec_custom("det", ctx=[3, 700, 40, 2000, 0], qlen=[1, 1, 33, 70, 100], num_decodes=2,
+                         num_extends=2, num_prefills=1, Hq=16, Hkv=2, d=128, dv=128, bs=16, chunk=512,
+                         seed=4)
+    out, lse, err, db = run_gpu(W.make_batch(spec))
+    first = db.out.clone()
+    db.forward()
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), db.out.view(torch.int16))
+
+
+# ---------------------------------------------------------------- error paths
+def _with_metadata(batch, **changes):
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    db = DeviceBatch(batch)
+    for k, v in changes.items():
+        getattr(db, k).copy_(v)
+    return db
+
+
+def test_device_error_order():
+    """A prefill placed in the decode slice: ORDER bit, nothing computed."""
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    spec = W.spec_custom("ord", ctx=[10, 0], qlen=[1, 5], num_decodes=1, num_extends=0, num_prefills=1,
+                         Hq=4, Hkv=2, d=64, dv=64, bs=16)
+    db = _with_metadata(W.make_batch(spec))
+    db.spec = W.spec_custom("ord", ctx=[10, 0], qlen=[1, 5], num_decodes=2, num_extends=0,
+                            num_prefills=0, Hq=4, Hkv=2, d=64, dv=64, bs=16)
+    db.workspace = torch.zeros(db.workspace.numel() + (4 << 20), dtype=torch.uint8, device="cuda")
+    db.out.fill_(7.0)
+    db.forward()
+    err = db.error_word()
+    assert err & pka.DEVERR["ORDER"]
+    assert torch.all(db.out == 7.0)  # no work was done
+
+
+def test_device_error_bad_block_id():
+    """A block id past the cache is flagged and never dereferenced."""
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    spec = W.spec_custom("blk", ctx=[40, 33], qlen=[1, 9], num_decodes=1, num_extends=1,
+                         num_prefills=0, Hq=4, Hkv=2, d=128, dv=128, bs=16, chunk=16)
+    batch = W.make_batch(spec)
+    db = _with_metadata(batch)
+    bt = db.block_table.clone()
+    bt[0, 1] = batch.num_blocks + 5
+    bt[1, 0] = -3
+    db.block_table.copy_(bt)
+    db.forward()
+    err = db.error_word()
+    assert err & pka.DEVERR["BLOCK_ID"]
+    assert err & ~(pka.DEVERR["BLOCK_ID"]) == 0
+
+
+def test_device_error_seq_len_hint():
+    """seq_len above the max_seq_len hint: SEQ_LEN bit, plan left empty."""
+    from paged_kv_attention_07_gb300 import pka
+    spec = W.spec_custom("sl", ctx=[40, 100], qlen=[1, 1], num_decodes=2, num_extends=0,
+                         num_prefills=0, Hq=4, Hkv=2, d=64, dv=64, bs=16)
+    db = _with_metadata(W.make_batch(spec))
+    db.max_seq_len = 50
+    db.forward()
+    assert db.error_word() & pka.DEVERR["SEQ_LEN"]
+
+
+def test_workspace_too_small_is_rejected():
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    spec = W.spec_tiny()
+    db = _with_metadata(W.make_batch(spec))
+    small = db.workspace[:1024]
+    with pytest.raises(pka.PkaError) as ei:
+        s = db.spec
+        pka.pka_paged_attn_forward(db.q, db.k_new, db.v_new, db.k_cache, db.v_cache, db.block_table,
+                                   db.qsl, db.seq_lens, s.num_decodes, s.num_extends, s.num_prefills,
+                                   s.scale, s.context_chunk, db.max_query_len, db.max_seq_len, db.out,
+                                   db.lse, small)
+    assert ei.value.status == 3
