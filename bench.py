@@ -309,6 +309,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
     peaks = load_peaks()
+    if args.workload != "decode_gqa":
+        return profile_workload(args, device)
     spec = W.spec_decode_gqa()
     db = make_device_batch(spec, device, seed=42 + rank)
     w = algorithmic_work(spec)
@@ -324,7 +326,7 @@ def run_ours(args):
                                                barrier=barrier)
     # keep the GPU busy long enough for the sampler to see the clocks under load
     extra_t0 = time.time()
-    while time.time() - extra_t0 < 1.0:
+    while args.clock_hold and time.time() - extra_t0 < 1.0:
         db.step()
     torch.cuda.synchronize()
     sampler.stop()
@@ -371,6 +373,20 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "prefill_varlen": W.spec_prefill, "mixed": W.spec_mixed,
+             "mla_decode_bs64": W.spec_mla_decode,
+             "mla_decode_bs1": lambda: W.spec_mla_decode(block_size=1)}
+
+
+def profile_workload(args, device):
+    """Run --steps steps of one workload and print its timing (for profilers)."""
+    spec = WORKLOADS[args.workload]()
+    db = make_device_batch(spec, device, seed=7)
+    ms, stats, launches, _ = time_steps(db, args.steps, args.warmup)
+    print(json.dumps({"workload": args.workload, "ms_per_step": ms,
+                      "kernels_ms": {k: v["avg_ms"] for k, v in stats.items()}, "gpu_launches": launches}))
+
+
 def run_reference(args):
     """The oracle (float64 C, host cores) as the reference arm, on a bounded
     sample of the same workload per step."""
@@ -411,7 +427,14 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--primary-only", dest="all_workloads", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_gqa",
+                    help="run only this workload's steps (for profilers); the default is the headline")
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for profilers: no clock hold, e2e, CPU baseline or secondary workloads")
     args = ap.parse_args()
+    args.clock_hold = True
+    if args.profile:
+        args.e2e = args.all_workloads = args.cpu_baseline = args.clock_hold = False
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
