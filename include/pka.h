@@ -205,6 +205,49 @@ PKA_API pka_status pka_merge_attn_states(void *out, float *out_lse, const void *
 PKA_API pka_status pka_get_error(const void *workspace, int32_t *code_out, void *stream);
 
 /*
+ * pka_paged_decode_noalloc -- the split-KV GQA decode of pka_paged_attn_forward
+ * for callers that cannot hand the library any scratch memory.
+ *
+ * The pages have no counterpart to this call; it exists for integration.
+ * Some callers cannot allocate device memory when they call into the
+ * library: a serving engine that reserved nearly all device memory for its
+ * KV-cache pool up front (a cudaMalloc would fail or fragment the pool), or
+ * a plugin host that gives its kernels no workspace and forbids allocation
+ * on the hot path because cudaMalloc/cudaFree synchronise the device. This
+ * entry point needs no workspace: its scratch (work lists, split partials,
+ * error word) is a fixed array of PKA_NOALLOC_SCRATCH_BYTES bytes compiled
+ * into the library as a static device variable, which every GPU that loads
+ * the library keeps until the process exits. It allocates nothing.
+ *
+ * Computes exactly what pka_paged_attn_forward computes for a batch of
+ * num_decodes decode requests (query_len 1 each, so num_tokens ==
+ * num_decodes), with the same argument meanings, layouts and supported GQA
+ * shapes ((head_dim, head_dim_v) in {(64, 64), (128, 128)}; v_cache must not
+ * be NULL). The cache must already hold the new tokens (pka_cache_write).
+ *
+ *   error_word  device int32 or NULL; receives the call's device error word
+ *               (PKA_DEVERR_*; 0 when clean) at the end of the call.
+ * Returns PKA_ERR_WORKSPACE_TOO_SMALL, launching nothing, when the batch
+ * needs more scratch than PKA_NOALLOC_SCRATCH_BYTES (with 32 query heads of
+ * dim 128, up to about 2000 decode requests fit).
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture. Every call on a device shares the one array, which keeps the last
+ * call's contents (the call clears what must start at zero), so calls whose
+ * work overlaps on the GPU -- on different streams, or from different host
+ * threads -- race and must be serialised by the caller.
+ */
+#define PKA_NOALLOC_SCRATCH_BYTES (32u << 20)
+PKA_API pka_status pka_paged_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                            const int32_t *block_table, int max_blocks_per_req,
+                                            const int32_t *query_start_loc, const int32_t *seq_lens,
+                                            int num_decodes, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int64_t num_blocks, int block_size,
+                                            float scale, int max_seq_len, void *out, float *lse,
+                                            int32_t *error_word, void *stream);
+
+/*
  * Kernel timing for benchmarks (not needed for normal use). While enabled,
  * every launch of the selected kernel family is bracketed by a CUDA event
  * pair recorded on the launching stream (events are created once and

@@ -173,6 +173,26 @@ cudaError_t timed(int kernel, cudaStream_t st, F&& launch) {
     return e;
 }
 
+// ---- scratch of pka_paged_decode_noalloc: a fixed device array, no allocation
+__device__ __align__(256) uint8_t g_noalloc_scratch[PKA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current (host code cannot use the symbol's
+// host-side name as a device pointer).
+uint8_t* noalloc_scratch() {
+    static std::mutex mu;
+    static uint8_t* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        addr[dev] = static_cast<uint8_t*>(p);
+    }
+    return addr[dev];
+}
+
 }  // namespace
 }  // namespace pka
 
@@ -489,6 +509,138 @@ pka_status pka_merge_attn_states(void* out, float* out_lse, const void* prefix_o
         return launch_merge_pair(out, out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse, num_rows, head_dim,
                                  io_dtype, sms, st);
     }));
+}
+
+pka_status pka_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_table, int max_blocks_per_req,
+                                    const int32_t* query_start_loc, const int32_t* seq_lens, int num_decodes,
+                                    int num_q_heads, int num_kv_heads, int head_dim, int64_t num_blocks,
+                                    int block_size, float scale, int max_seq_len, void* out, float* lse,
+                                    int32_t* error_word, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (num_decodes < 1) return num_decodes == 0 ? PKA_OK : PKA_ERR_INVALID_ARG;
+    bool is_mla = false;
+    pka_status sc = check_shape(num_decodes, 0, 0, num_decodes, num_q_heads, num_kv_heads, head_dim, head_dim,
+                                1, max_seq_len, 16, false, &is_mla);
+    if (sc != PKA_OK) return sc;
+    if (!q || !k_cache || !v_cache || !block_table || !query_start_loc || !seq_lens || !out)
+        return PKA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        (lse && !aligned(lse, 4)) || (error_word && !aligned(error_word, 4)))
+        return PKA_ERR_INVALID_ARG;
+    if (max_blocks_per_req <= 0 || num_blocks <= 0 || !pow2(block_size) || block_size > 128)
+        return block_size > 128 || !pow2(block_size) ? PKA_ERR_UNSUPPORTED : PKA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKA_ERR_INVALID_ARG;
+    const int64_t cache_rows = num_blocks * num_kv_heads * (int64_t)block_size;
+    if (cache_rows >= (int64_t)INT32_MAX) return PKA_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_req * block_size < max_seq_len) return PKA_ERR_INVALID_ARG;
+
+    // Scratch layout inside the fixed array: header, pairs, per-request
+    // split index, then the split partials. The number of split pairs is
+    // capped so everything fits; a batch that cannot fit is rejected.
+    const int Hq = num_q_heads, dv = head_dim, nd = num_decodes;
+    const size_t per_pair = sizeof(int2) + (size_t)Hq * dv * sizeof(float) + (size_t)Hq * sizeof(float);
+    const size_t fixed = sizeof(PlanHeader) + 2 * align256((size_t)nd * sizeof(int32_t)) + 5 * 256;
+    if (fixed >= PKA_NOALLOC_SCRATCH_BYTES) return PKA_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t cap = (int64_t)((PKA_NOALLOC_SCRATCH_BYTES - fixed) / per_pair);
+    if (cap < (int64_t)nd + 2) return PKA_ERR_WORKSPACE_TOO_SMALL;
+    const int sms = device_sm_count();
+    if (sms <= 0) return PKA_ERR_CUDA;
+    int64_t target = std::min<int64_t>(decode_gqa_target_units(sms), (cap - nd - 1) * (int64_t)num_kv_heads);
+    if (target < num_kv_heads) return PKA_ERR_WORKSPACE_TOO_SMALL;
+    const int pair_cap = (int)(target / num_kv_heads + nd + 1);
+    size_t off = sizeof(PlanHeader);
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align256(off + bytes);
+        return o;
+    };
+    const size_t off_pairs = take(sizeof(int2) * (size_t)pair_cap);
+    const size_t off_first = take(sizeof(int32_t) * (size_t)nd);
+    const size_t off_nsplit = take(sizeof(int32_t) * (size_t)nd);
+    const size_t off_po = take(sizeof(float) * (size_t)pair_cap * Hq * dv);
+    const size_t off_pl = take(sizeof(float) * (size_t)pair_cap * Hq);
+    if (off > PKA_NOALLOC_SCRATCH_BYTES) return PKA_ERR_WORKSPACE_TOO_SMALL;
+
+    uint8_t* ws = noalloc_scratch();
+    if (!ws) return PKA_ERR_CUDA;
+    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
+    // the header (error word, counters) must start at zero on every call
+    if (cudaMemsetAsync(hdr, 0, sizeof(PlanHeader), st) != cudaSuccess) return PKA_ERR_CUDA;
+
+    PlanParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.qsl = query_start_loc;
+    pp.seq_lens = seq_lens;
+    pp.num_decodes = nd;
+    pp.num_tokens = nd;
+    pp.max_query_len = 1;
+    pp.max_seq_len = max_seq_len;
+    pp.max_blocks_per_req = max_blocks_per_req;
+    pp.block_size = block_size;
+    pp.chunk = 16;
+    pp.dec_units_per_pair = num_kv_heads;
+    pp.dec_target_units = (int)target;
+    pp.dec_min_split = kDecodeMinSplit;
+    pp.dec_pair_cap = pair_cap;
+    pp.hdr = hdr;
+    pp.dec_pairs = reinterpret_cast<int2*>(ws + off_pairs);
+    pp.dec_first = reinterpret_cast<int32_t*>(ws + off_first);
+    pp.dec_nsplit = reinterpret_cast<int32_t*>(ws + off_nsplit);
+    if (launch_planner(pp, st) != cudaSuccess) return PKA_ERR_CUDA;
+
+    const bool tma = block_size >= 8;
+    CUtensorMap km, vm;
+    std::memset(&km, 0, sizeof(km));
+    std::memset(&vm, 0, sizeof(vm));
+    if (tma) {
+        const uint32_t br = (uint32_t)std::min(block_size, 16);
+        if (!encode_rows(&km, k_cache, (uint64_t)cache_rows, head_dim, br) ||
+            !encode_rows(&vm, v_cache, (uint64_t)cache_rows, head_dim, br))
+            return PKA_ERR_CUDA;
+    }
+    auto* outb = static_cast<__nv_bfloat16*>(out);
+    float* po = reinterpret_cast<float*>(ws + off_po);
+    float* pl = reinterpret_cast<float*>(ws + off_pl);
+    DecodeGqaParams dp;
+    dp.q = static_cast<const __nv_bfloat16*>(q);
+    dp.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+    dp.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+    dp.block_table = block_table;
+    dp.seq_lens = seq_lens;
+    dp.hdr = hdr;
+    dp.counter = &hdr->dec_counter;
+    dp.err = &hdr->err;
+    dp.pairs = pp.dec_pairs;
+    dp.nsplit = pp.dec_nsplit;
+    dp.part_o = po;
+    dp.part_lse = pl;
+    dp.out = outb;
+    dp.lse = lse;
+    dp.num_blocks = num_blocks;
+    dp.max_blocks = max_blocks_per_req;
+    dp.Hq = Hq;
+    dp.Hkv = num_kv_heads;
+    dp.G = Hq / num_kv_heads;
+    dp.bs = block_size;
+    dp.scale_log2 = scale * 1.4426950408889634f;
+    if (launch_decode_gqa(km, vm, dp, head_dim, tma, sms, st) != cudaSuccess) return PKA_ERR_CUDA;
+    DecodeReduceParams rp;
+    rp.hdr = hdr;
+    rp.dec_first = pp.dec_first;
+    rp.dec_nsplit = pp.dec_nsplit;
+    rp.part_o = po;
+    rp.part_lse = pl;
+    rp.out = outb;
+    rp.lse = lse;
+    rp.num_decodes = nd;
+    rp.Hq = Hq;
+    rp.dv = dv;
+    if (launch_decode_reduce(rp, sms, st) != cudaSuccess) return PKA_ERR_CUDA;
+    if (error_word &&
+        cudaMemcpyAsync(error_word, &hdr->err, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return PKA_ERR_CUDA;
+    return PKA_OK;
 }
 
 pka_status pka_kernel_timer(int kernel, int enable) {

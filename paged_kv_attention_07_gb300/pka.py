@@ -19,8 +19,8 @@ STATUS_NAMES = {0: "PKA_OK", 1: "PKA_ERR_INVALID_ARG", 2: "PKA_ERR_UNSUPPORTED",
 DEVERR = {"QUERY_START_LOC": 0x01, "SEQ_LEN": 0x02, "ORDER": 0x04, "QUERY_LEN": 0x08,
           "BLOCK_TABLE": 0x10, "BLOCK_ID": 0x20, "SLOT": 0x40, "CAPACITY": 0x80, "TIMEOUT": 0x100}
 EXPORTED = ("pka_cache_write", "pka_workspace_size", "pka_paged_attn_forward",
-            "pka_merge_attn_states", "pka_get_error", "pka_kernel_timer", "pka_kernel_timer_read",
-            "pka_status_string")
+            "pka_merge_attn_states", "pka_get_error", "pka_paged_decode_noalloc", "pka_kernel_timer",
+            "pka_kernel_timer_read", "pka_status_string")
 KERNELS = {"cache_write": 0, "planner": 1, "decode": 2, "decode_reduce": 3, "prefill_extend": 4,
            "extend_reduce": 5, "merge": 6}
 
@@ -60,6 +60,9 @@ def load(path: str | None = None):
     lib.pka_merge_attn_states.argtypes = [P, P, P, P, P, P, i64, i32, i32, P]
     lib.pka_get_error.restype = i32
     lib.pka_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32), P]
+    lib.pka_paged_decode_noalloc.restype = i32
+    lib.pka_paged_decode_noalloc.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, i64, i32, f32, i32,
+                                             P, P, P, P]
     lib.pka_kernel_timer.restype = i32
     lib.pka_kernel_timer.argtypes = [i32, i32]
     lib.pka_kernel_timer_read.restype = i32
