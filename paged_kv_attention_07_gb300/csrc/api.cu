@@ -25,7 +25,7 @@ cudaError_t launch_decode_gqa(const CUtensorMap& km, const CUtensorMap& vm, cons
                               int head_dim, bool tma, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode_mla(const CUtensorMap& map, const DecodeMlaParams& p, bool tma, int num_sms,
                               cudaStream_t stream);
-cudaError_t launch_fa_fwd(const FaParams& p, int head_dim, int num_sms, cudaStream_t stream);
+cudaError_t launch_fa_fwd(const FaMaps& maps, const FaParams& p, int head_dim, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode_reduce(const DecodeReduceParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bound, int num_sms,
                                  cudaStream_t stream);
@@ -79,6 +79,21 @@ bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 view of a token-major tensor [T, H, D] read in boxes of
+// 64 columns x 1 head x 128 tokens (128-byte swizzle): one box gives 128
+// consecutive tokens of one head, 128 bytes per token.
+bool encode_tokens(CUtensorMap* map, const void* base, uint64_t T, uint64_t H, uint64_t D) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {D, H, T};
+    cuuint64_t strides[2] = {D * 2, H * D * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -464,8 +479,20 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
         fp.num_decodes = num_decodes;
         fp.num_extends = num_extends;
         fp.scale_log2 = scale_log2;
-        if ((e = timed(PKA_KERNEL_PREFILL_EXTEND, st, [&] { return launch_fa_fwd(fp, head_dim, sms, st); })) !=
-            cudaSuccess)
+        FaMaps maps;
+        std::memset(&maps, 0, sizeof(maps));
+        if (!encode_tokens(&maps.q, q, (uint64_t)num_tokens, num_q_heads, head_dim) ||
+            !encode_tokens(&maps.knew, k_new, (uint64_t)num_tokens, num_kv_heads, head_dim) ||
+            !encode_tokens(&maps.vnew, v_new, (uint64_t)num_tokens, num_kv_heads, head_dim_v))
+            return PKA_ERR_CUDA;
+        if (block_size >= 8) {
+            const uint32_t br = (uint32_t)std::min(block_size, 128);
+            if (!encode_rows(&maps.kc, k_cache, (uint64_t)cache_rows, head_dim, br) ||
+                !encode_rows(&maps.vc, v_cache, (uint64_t)cache_rows, head_dim_v, br))
+                return PKA_ERR_CUDA;
+        }
+        if ((e = timed(PKA_KERNEL_PREFILL_EXTEND, st,
+                       [&] { return launch_fa_fwd(maps, fp, head_dim, sms, st); })) != cudaSuccess)
             return PKA_ERR_CUDA;
         if (num_extends > 0) {
             ExtendReduceParams xp;

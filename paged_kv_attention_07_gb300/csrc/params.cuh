@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 #include "plan.cuh"
 
 namespace pka {
@@ -92,6 +94,14 @@ struct ExtendReduceParams {
     __nv_bfloat16* out;
     float* lse;
     int num_decodes, num_extends, Hq, dv, chunk;
+};
+
+struct FaMaps {
+    CUtensorMap q;     // [T, Hq, D]  box {64, 1, 128}
+    CUtensorMap knew;  // [T, Hkv, D] box {64, 1, 128}
+    CUtensorMap vnew;
+    CUtensorMap kc;    // [nb * Hkv * bs, D] box {64, min(bs, 128)}
+    CUtensorMap vc;
 };
 
 }  // namespace pka

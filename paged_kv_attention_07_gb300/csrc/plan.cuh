@@ -20,8 +20,8 @@ namespace pka {
 
 constexpr int kMaxRequests = 4096;     // planner keeps per-request metadata in smem
 constexpr int kDecodeMinSplit = 256;   // fewest keys per GQA decode split
-constexpr int kFaBlockM = 64;          // query rows per prefill/extend item
-constexpr int kFaBlockN = 64;          // keys per prefill/extend tile (cost unit)
+constexpr int kFaBlockM = 128;         // query rows per prefill/extend item (TMEM lanes)
+constexpr int kFaBlockN = 128;         // keys per prefill/extend tile (cost unit)
 constexpr int kCostBuckets = 1024;
 
 struct PlanHeader {

@@ -116,12 +116,15 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
         for (int s = 0; s < n; ++s) p.dec_pairs[base + s] = make_int2(r, s);
     }
 
-    // ---- prefill / extend items, counting-sorted by cost (heaviest first)
-    auto item_cost = [&](int r, int qt, int slot) -> int {
+    // ---- prefill / extend items. A group is one (request, slot): all query
+    // tiles that read the same keys. Groups are counting-sorted by the cost of
+    // their heaviest tile (heaviest first) and keep their tiles contiguous, so
+    // the CTAs that share a context chunk stream it through L2 together.
+    auto group_cost = [&](int r, int slot) -> int {
         const int ql = s_qlen[r];
         int keys;
         if (slot == 0) {
-            keys = min(ql, (qt + 1) * kFaBlockM);
+            keys = ql;  // the last query tile sees all new keys
         } else {
             const int ctx = s_slen[r] - ql;
             keys = min(p.chunk, ctx - (slot - 1) * p.chunk);
@@ -134,8 +137,7 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
         const int ctx = s_slen[r] - ql;
         const int nqt = (ql + kFaBlockM - 1) / kFaBlockM;
         const int nslot = (r < nd + ne) ? 1 + (ctx + p.chunk - 1) / p.chunk : 1;
-        for (int qt = 0; qt < nqt; ++qt)
-            for (int s = 0; s < nslot; ++s) atomicAdd(&s_hist[item_cost(r, qt, s)], 1);
+        for (int s = 0; s < nslot; ++s) atomicAdd(&s_hist[group_cost(r, s)], nqt);
     }
     __syncthreads();
     if (tid == 0) {
@@ -164,12 +166,12 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
         const int ctx = s_slen[r] - ql;
         const int nqt = (ql + kFaBlockM - 1) / kFaBlockM;
         const int nslot = (r < nd + ne) ? 1 + (ctx + p.chunk - 1) / p.chunk : 1;
-        for (int qt = 0; qt < nqt; ++qt)
-            for (int s = 0; s < nslot; ++s) {
-                const int c = item_cost(r, qt, s);
-                const int pos = atomicAdd(&s_hist[c], 1);
-                p.fa_items[pos] = make_int4(r, qt, s, c);
-            }
+        for (int s = 0; s < nslot; ++s) {
+            const int c = group_cost(r, s);
+            const int pos = atomicAdd(&s_hist[c], nqt);
+            // causal groups: heaviest (last) query tile first
+            for (int qt = 0; qt < nqt; ++qt) p.fa_items[pos + qt] = make_int4(r, s == 0 ? nqt - 1 - qt : qt, s, c);
+        }
     }
     if (tid == 0) {
         p.hdr->dec_split_len = L;
