@@ -32,6 +32,8 @@ cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bou
 int decode_gqa_target_units(int num_sms);
 int decode_mla_heads_per_cta(int Hq);
 
+static int mla_units_per_pair(int Hq) { return Hq / decode_mla_heads_per_cta(Hq); }
+
 namespace {
 
 constexpr int kMlaMinSplit = 1024;
@@ -116,7 +118,7 @@ bool compute_layout(const Hints& h, int num_sms, Layout* L) {
         off = align256(off + bytes);
         return o;
     };
-    const int upp = h.mla ? h.Hq / decode_mla_heads_per_cta(h.Hq) : h.Hkv;
+    const int upp = h.mla ? mla_units_per_pair(h.Hq) : h.Hkv;
     L->dec_target_units = h.mla ? num_sms * 4 : decode_gqa_target_units(num_sms);
     if (L->dec_target_units < 1) L->dec_target_units = 1;
     const int64_t pair_cap = h.nd > 0 ? (int64_t)L->dec_target_units / upp + h.nd + 1 : 0;
@@ -346,9 +348,10 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
     pp.max_blocks_per_req = max_blocks_per_req;
     pp.block_size = block_size;
     pp.chunk = context_chunk_tokens;
-    pp.dec_units_per_pair = is_mla ? num_q_heads / decode_mla_heads_per_cta(num_q_heads) : num_kv_heads;
+    pp.dec_units_per_pair = is_mla ? mla_units_per_pair(num_q_heads) : num_kv_heads;
     pp.dec_target_units = L.dec_target_units;
     pp.dec_min_split = is_mla ? kMlaMinSplit : kDecodeMinSplit;
+    pp.dec_split_align = 16;
     pp.dec_pair_cap = L.dec_pair_cap;
     pp.fa_item_cap = L.fa_item_cap;
     pp.ext_row_cap = L.ext_row_cap;
@@ -609,6 +612,7 @@ pka_status pka_paged_decode_noalloc(const void* q, const void* k_cache, const vo
     pp.dec_units_per_pair = num_kv_heads;
     pp.dec_target_units = (int)target;
     pp.dec_min_split = kDecodeMinSplit;
+    pp.dec_split_align = 16;
     pp.dec_pair_cap = pair_cap;
     pp.hdr = hdr;
     pp.dec_pairs = reinterpret_cast<int2*>(ws + off_pairs);

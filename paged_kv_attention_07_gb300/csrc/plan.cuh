@@ -51,6 +51,7 @@ struct PlanParams {
     int dec_units_per_pair;  // kv heads (GQA) or head groups (MLA) per pair
     int dec_target_units;
     int dec_min_split;       // fewest keys per decode split
+    int dec_split_align;     // split length is a multiple of this (the kernel's key tile)
     int dec_pair_cap, fa_item_cap, ext_row_cap;
     PlanHeader* hdr;
     int2* dec_pairs;

@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
         if (nd > 0) {
             const unsigned long long units = s_dec_keys * (unsigned long long)p.dec_units_per_pair;
             unsigned long long want = (units + p.dec_target_units - 1) / (unsigned long long)p.dec_target_units;
-            want = (want + 15ull) & ~15ull;
+            const unsigned long long a = (unsigned long long)p.dec_split_align;
+            want = (want + a - 1) / a * a;
             if (want > (unsigned long long)L) L = (int)(want > (1ull << 30) ? (1ull << 30) : want);
         }
         int pairs = 0;

@@ -69,6 +69,14 @@ def test_decode_mla(Hq, bs):
     check_batch(W.make_batch(spec))
 
 
+def test_decode_mla_many_units():
+    """More (request, split, half) units than SMs, several splits per request."""
+    rng = np.random.default_rng(17)
+    ctx = rng.integers(1, 2500, 192).tolist()
+    spec = _dec("mla_many", ctx, 128, 1, 576, 64, seed=17, mla=True, dv=512)
+    check_batch(W.make_batch(spec))
+
+
 def test_constant_v_gives_constant_output():
     spec = W.spec_custom("const", ctx=[0, 90, 30, 0], qlen=[1, 1, 20, 50], num_decodes=2,
                          num_extends=1, num_prefills=1, Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=32)
