@@ -13,13 +13,14 @@
 //
 // Work unit: (request, 128-row query tile, slot) x query head, slot 0 = new
 // keys, slot c >= 1 = context chunk c - 1. Persistent CTAs (one per SM) walk
-// the planner's cost-sorted unit list round-robin. Per CTA, 7 warps:
+// the planner's cost-sorted unit list round-robin. Per CTA, 8 warps:
 //   warps 0, 6 TMA producers: warp 0 the Q tile (double-buffered) and K
 //            tiles of 128 keys, warp 6 the V tiles, each into a 2-stage ring
 //            (block sizes below 8 use cp.async copies);
-//   warp 1   MMA issuer (one thread) and tensor-memory owner:
-//            S = Q K^T into one of two TMEM S buffers (128 fp32 columns each),
-//            O += P V into a TMEM O accumulator (head_dim fp32 columns);
+//   warp 1   tensor-memory owner; one thread issues S = Q K^T into one of
+//            two TMEM S buffers (128 fp32 columns each), running ahead;
+//   warp 7   one thread issues O += P V into the TMEM O accumulator
+//            (head_dim fp32 columns) as soon as each P is written;
 //   warps 2-5 softmax warpgroup, one thread per query row (= TMEM lane):
 //            reads its S row, masks, keeps the running max and sum in
 //            registers, writes P (bf16 pairs) into one of two TMEM P buffers
@@ -39,7 +40,7 @@
 
 namespace pka {
 
-constexpr int kFaThreads = 224;
+constexpr int kFaThreads = 256;
 constexpr int BM = kFaBlockM;  // 128 query rows per unit
 constexpr int BN = kFaBlockN;  // 128 keys per tile
 static_assert(BM == 128 && BN == 128, "tile shape is fixed by the TMEM lane count");
@@ -254,36 +255,18 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         }
         if (which == 0)
             for (uint32_t k = q_it > 2 ? q_it - 2 : 0; k < q_it; ++k) mbar_wait(&q_full[k & 1], (k >> 1) & 1, p.err);
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+    } else if (warp == 1 || warp == 7) {
+        // ------------------------------------------------------------ MMA issuers
+        // warp 1 streams S = Q K^T ahead of the softmax (gated only by a free S
+        // buffer and the K tile); warp 7 issues O += P V as each P lands. Each
+        // thread commits only its own MMAs.
+        if (lane == 0 && warp == 1) {
             constexpr uint32_t idesc_qk = umma_idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, 0, 1);
-            const uint32_t q_s = sm_base + C::kOffQ, k_s = sm_base + C::kOffK, v_s = sm_base + C::kOffV;
-            uint32_t kv_it = 0, s_it = 0, pv_it = 0, q_it = 0;
+            const uint32_t q_s = sm_base + C::kOffQ, k_s = sm_base + C::kOffK;
+            uint32_t kv_it = 0, s_it = 0, q_it = 0;
             bool ok = true;
-            // O (+)= P_t . V_t ; P buffer and its barriers alternate with the global PV count
-            auto issue_pv = [&](int t, uint32_t kv_base) -> bool {
-                const uint32_t vi = kv_base + t;
-                const int vs = vi & 1;
-                const int pb = pv_it & 1;
-                if (!mbar_wait(&p_full[pb], (pv_it >> 1) & 1, p.err)) return false;
-                if (!mbar_wait(&v_full[vs], (vi >> 1) & 1, p.err)) return false;
-                if (t == 0 && q_it > 0 && !mbar_wait(o_free, (q_it - 1) & 1, p.err)) return false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t b = umma_desc_sw128(v_s + vs * C::kKVBytes + kk * 2048, C::kChunkBytes, 1024);
-                    umma_bf16_ts(tbase + C::kColO, tbase + C::kColP + pb * 64 + kk * 8, b, idesc_pv,
-                                 (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                umma_commit(&pv_done[pb]);
-                umma_commit(&v_empty[vs]);
-                ++pv_it;
-                return true;
-            };
             FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
-            for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x) {
+            for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x, ++q_it) {
                 const FaUnit U = Un;
                 if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
                 const int qb = q_it & 1;
@@ -291,7 +274,6 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     ok = false;
                     break;
                 }
-                const uint32_t kv_base = kv_it;
                 for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
                     const int st = kv_it & 1;
                     const int b = s_it & 1;
@@ -309,11 +291,37 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     umma_commit(&k_empty[st]);
                     if (t == U.ntiles - 1) umma_commit(&q_empty[qb]);
                     ++s_it;
-                    if (t > 0 && !issue_pv(t - 1, kv_base)) { ok = false; break; }
                 }
-                if (!ok) break;
-                if (!issue_pv(U.ntiles - 1, kv_base)) { ok = false; break; }
-                ++q_it;
+            }
+            if (!ok) s_abort = 1;
+            if (s_it > 0) mbar_wait(&s_full[(s_it - 1) & 1], ((s_it - 1) >> 1) & 1, p.err);
+        } else if (lane == 0 && warp == 7) {
+            constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, 0, 1);
+            const uint32_t v_s = sm_base + C::kOffV;
+            uint32_t kv_it = 0, pv_it = 0, q_it = 0;
+            bool ok = true;
+            FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
+            for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x, ++q_it) {
+                const FaUnit U = Un;
+                if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
+                for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
+                    const int vs = kv_it & 1;
+                    const int pb = pv_it & 1;
+                    if (!mbar_wait(&p_full[pb], (pv_it >> 1) & 1, p.err)) { ok = false; break; }
+                    if (!mbar_wait(&v_full[vs], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                    // the first product of a unit overwrites O: the previous unit's O must be read
+                    if (t == 0 && q_it > 0 && !mbar_wait(o_free, (q_it - 1) & 1, p.err)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t bdesc = umma_desc_sw128(v_s + vs * C::kKVBytes + kk * 2048, C::kChunkBytes, 1024);
+                        umma_bf16_ts(tbase + C::kColO, tbase + C::kColP + pb * 64 + kk * 8, bdesc, idesc_pv,
+                                     (t > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&pv_done[pb]);
+                    umma_commit(&v_empty[vs]);
+                    ++pv_it;
+                }
             }
             if (!ok) s_abort = 1;
             // let every issued MMA finish before the CTA can exit
