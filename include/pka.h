@@ -150,7 +150,7 @@ PKA_API size_t pka_workspace_size(int num_decodes, int num_extends, int num_pref
  *                   num_extends + num_prefills
  *   query_start_loc device, [B + 1] int32
  *   seq_lens        device, [B] int32 (cached + new tokens)
- *   scale           multiplies q.k (e.g. 1/sqrt(head_dim))
+ *   scale           multiplies q.k (e.g. 1/sqrt(head_dim)); finite and > 0, else PKA_ERR_INVALID_ARG
  *   context_chunk_tokens  context tokens per extend chunk (the pages' ~32K
  *                   per-iteration budget), >= 16
  *   max_query_len, max_seq_len  host upper bounds of query_len and seq_len

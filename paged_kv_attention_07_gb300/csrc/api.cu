@@ -317,7 +317,7 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
         return PKA_ERR_INVALID_ARG;
     if (max_blocks_per_req <= 0 || num_blocks <= 0 || !pow2(block_size) || block_size > 128)
         return block_size > 128 || !pow2(block_size) ? PKA_ERR_UNSUPPORTED : PKA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return PKA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return PKA_ERR_INVALID_ARG;  // masking and the row max assume scale > 0
     const int64_t cache_rows = num_blocks * num_kv_heads * (int64_t)block_size;
     if (cache_rows >= (int64_t)INT32_MAX) return PKA_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_req * block_size < max_seq_len) return PKA_ERR_INVALID_ARG;
@@ -560,7 +560,7 @@ pka_status pka_paged_decode_noalloc(const void* q, const void* k_cache, const vo
         return PKA_ERR_INVALID_ARG;
     if (max_blocks_per_req <= 0 || num_blocks <= 0 || !pow2(block_size) || block_size > 128)
         return block_size > 128 || !pow2(block_size) ? PKA_ERR_UNSUPPORTED : PKA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return PKA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return PKA_ERR_INVALID_ARG;  // masking and the row max assume scale > 0
     const int64_t cache_rows = num_blocks * num_kv_heads * (int64_t)block_size;
     if (cache_rows >= (int64_t)INT32_MAX) return PKA_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_req * block_size < max_seq_len) return PKA_ERR_INVALID_ARG;

@@ -13,26 +13,31 @@
 //
 // Work unit: (request, 128-row query tile, slot) x query head, slot 0 = new
 // keys, slot c >= 1 = context chunk c - 1. Persistent CTAs (one per SM) walk
-// the planner's cost-sorted unit list round-robin. Per CTA, 8 warps:
-//   warps 0, 6 TMA producers: warp 0 the Q tile (double-buffered) and K
-//            tiles of 128 keys, warp 6 the V tiles, each into a 2-stage ring
-//            (block sizes below 8 use cp.async copies);
-//   warp 1   tensor-memory owner; one thread issues S = Q K^T into one of
-//            two TMEM S buffers (128 fp32 columns each), running ahead;
-//   warp 7   one thread issues O += P V into the TMEM O accumulator
-//            (head_dim fp32 columns) as soon as each P is written;
-//   warps 2-5 softmax warpgroup, one thread per query row (= TMEM lane):
-//            reads its S row, masks, keeps the running max and sum in
-//            registers, writes P (bf16 pairs) into one of two TMEM P buffers
-//            (the P . V product takes its A operand from TMEM), rescales its
-//            O row in TMEM only when the max grew by more than 2^8
-//            (otherwise the stale max is kept: P stays <= 2^8), and finally
-//            reads O, divides by the sum and stores out (+ LSE).
-// TMEM holds S0, S1, O, P0, P1 (512 columns). Q, S and P are
-// double-buffered: while the softmax works on tile j the tensor core
-// computes S_{j+1} and O += P_{j-1} V_{j-1}, and the next unit's Q loads
-// during the current one. Every barrier that could complete twice before
-// its waiter looks exists per buffer, so mbarrier phase parities never alias.
+// the planner's cost-sorted unit list round-robin. Per CTA, 12 warps:
+//   warp 0   TMA producer of the Q tile (double-buffered) and the K tiles of
+//            128 keys (2-stage ring); warp 2 the same for the V tiles (block
+//            sizes below 8 use cp.async copies);
+//   warp 1   tensor-memory owner; one thread issues S = Q K^T;
+//   warp 3   one thread issues O += P V (A operand P read from TMEM);
+//   warps 4-7, 8-11: two softmax warpgroups, one thread per query row (=
+//            TMEM lane). Warpgroup k takes the unit's key tiles t = k, k+2,
+//            ... with its own S buffer S_k, its own running max and sum and
+//            its own accumulator O_k, so one warpgroup's exponentials overlap
+//            the other's waits, loads and stores. Each reads its S row twice
+//            (row max, then exponentials: the row never has to sit in
+//            registers whole), writes P as bf16 pairs over the S_k columns it
+//            has already consumed, and rescales O_k only when its max grew by
+//            more than 2^8 (otherwise the stale max is kept: P stays <= 2^8).
+//            At the end of a unit the two (max, sum, O) are merged exactly
+//            like two KV splits (the LSE merge), each warpgroup producing half
+//            of the head_dim columns of out (+ LSE).
+// TMEM holds S0, S1 (128 fp32 columns each) and O0, O1 (head_dim fp32 columns
+// each): 512 columns. The S = Q K^T that refills S_k waits for the P . V that
+// read P_k, so a warpgroup that sees its S tile may also touch O_k freely.
+// Every barrier belongs to one buffer or one warpgroup and cannot complete
+// twice before its waiter looks, so mbarrier phase parities never alias.
+#include <type_traits>
+
 #include "common.cuh"
 #include "params.cuh"
 #include "plan.cuh"
@@ -40,7 +45,7 @@
 
 namespace pka {
 
-constexpr int kFaThreads = 256;
+constexpr int kFaThreads = 384;
 constexpr int BM = kFaBlockM;  // 128 query rows per unit
 constexpr int BN = kFaBlockN;  // 128 keys per tile
 static_assert(BM == 128 && BN == 128, "tile shape is fixed by the TMEM lane count");
@@ -56,8 +61,9 @@ struct FaCfg {
     static constexpr int kOffV = kOffK + 2 * kKVBytes;
     static constexpr int kOffBar = kOffV + 2 * kKVBytes;
     static constexpr int kSmem = kOffBar + 256 + 1024;
-    // TMEM columns: S0, S1 (fp32 128 each), O (fp32 D), P0, P1 (bf16x2, 64 each)
-    static constexpr uint32_t kColS = 0, kColO = 256, kColP = 384, kTmemCols = 512;
+    // TMEM columns: S0, S1 (fp32 128 each; P_k overwrites the first 64 columns
+    // of S_k as bf16 pairs), O0, O1 (fp32 D each)
+    static constexpr uint32_t kColS = 0, kColO = 256, kTmemCols = 512;
 };
 
 struct FaUnit {
@@ -109,19 +115,20 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-    uint64_t* q_full = bars + 0;    // [2] per Q buffer
-    uint64_t* q_empty = bars + 2;   // [2]
-    uint64_t* k_full = bars + 4;    // [2] per K stage
-    uint64_t* k_empty = bars + 6;   // [2]
-    uint64_t* v_full = bars + 8;    // [2] per V stage
-    uint64_t* v_empty = bars + 10;  // [2]
-    uint64_t* s_full = bars + 12;   // [2] per S buffer
-    uint64_t* s_free = bars + 14;   // [2]
-    uint64_t* p_full = bars + 16;   // [2] per P buffer
-    uint64_t* pv_done = bars + 18;  // [2] per P buffer: the P . V that read it is done
-    uint64_t* o_free = bars + 20;
+    uint64_t* q_full = bars + 0;     // [2] per Q buffer
+    uint64_t* q_empty = bars + 2;    // [2]
+    uint64_t* k_full = bars + 4;     // [2] per K stage
+    uint64_t* k_empty = bars + 6;    // [2]
+    uint64_t* v_full = bars + 8;     // [2] per V stage
+    uint64_t* v_empty = bars + 10;   // [2]
+    uint64_t* s_full = bars + 12;    // [2] per softmax warpgroup: its S tile is in TMEM
+    uint64_t* p_full = bars + 14;    // [2] its P is in TMEM (4 warp arrivals)
+    uint64_t* pv_done = bars + 16;   // [2] the P . V that read its P is done
+    uint64_t* o_free = bars + 18;    // the unit's epilogue has read O0 and O1 (8 warp arrivals)
+    uint64_t* ml_ready = bars + 19;  // both warpgroups' row max and sum are published (8 warp arrivals)
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
+    __shared__ float2 s_ml[2][2][BM];  // [unit parity][warpgroup][row] = (max, sum)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_units = p.hdr->fa_num_items * p.Hq;
@@ -136,11 +143,11 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
         }
-        mbar_init(o_free, 4);
+        mbar_init(o_free, 8);
+        mbar_init(ml_ready, 8);
         fence_barrier_init();
         s_abort = 0;
         tma_prefetch_desc(&maps.q);
@@ -156,9 +163,9 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
     const uint32_t tbase = s_tmem;
     const uint32_t sm_base = smem_u32(smem);
 
-    if (warp == 0 || warp == 6) {
+    if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers
-        // warp 0 loads Q and K tiles, warp 6 loads V tiles (so a V load that
+        // warp 0 loads Q and K tiles, warp 2 loads V tiles (so a V load that
         // waits for an older P . V never delays the next K). K/V lines stay
         // in L2 with normal priority: every context chunk is read by all the
         // query heads of its KV head and all query tiles of its request.
@@ -193,58 +200,56 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 const int kb = U.kb0 + t * BN;
                 const int blk_mine = blk_next;  // block ids of this tile, one per lane
                 if (paged_tma && t + 1 < U.ntiles) blk_next = tile_block_id(p, bt, kb + BN, U.c1, lane);
-                {
-                    uint64_t* full = which ? &v_full[st] : &k_full[st];
-                    uint64_t* empty = which ? &v_empty[st] : &k_empty[st];
-                    if (n > 0 && !mbar_wait(empty, (n - 1) & 1, p.err)) {
-                        s_abort = 1;
-                        ok = false;
-                        continue;
-                    }
-                    uint8_t* dst = smem + (which ? C::kOffV : C::kOffK) + st * C::kKVBytes;
-                    if (U.slot == 0) {
-                        if (lane == 0) {
-                            mbar_arrive_expect_tx(full, C::kKVBytes);
-                            for (int c = 0; c < C::kChunks; ++c)
-                                tma_load_3d(dst + c * C::kChunkBytes, which ? &maps.vnew : &maps.knew, full, c * 64,
-                                            U.g, U.q0 + kb, pol_kv);
-                        }
-                    } else if (ctx_tma) {
-                        // one lane per block issues that block's boxes (in parallel)
-                        const int bs = p.bs;
-                        const int nvalid = min(BN / bs, (U.c1 - kb + bs - 1) / bs);
-                        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nvalid * C::kChunks * bs * 128));
-                        __syncwarp();
-                        if (lane < nvalid) {
-                            const int row = (blk_mine * p.Hkv + U.g) * bs;
-                            for (int c = 0; c < C::kChunks; ++c)
-                                tma_load_2d(dst + c * C::kChunkBytes + lane * bs * 128, which ? &maps.vc : &maps.kc,
-                                            full, c * 64, row, pol_kv);
-                        }
-                    } else {
-                        // small blocks: 16-byte copies, rows past the chunk end zero-filled
-                        const uint32_t dbase = smem_u32(dst);
-                        const __nv_bfloat16* src_base = which ? p.v_cache : p.k_cache;
-                        for (int ci = lane; ci < BN * (D / 8); ci += 32) {
-                            const int row = ci / (D / 8), c = ci % (D / 8);
-                            const int pos = kb + row;
-                            const bool valid = pos < U.c1;
-                            int blk = valid ? __ldg(bt + pos / p.bs) : 0;
-                            if (blk < 0 || blk >= p.num_blocks) {
-                                set_error(p.err, PKA_DEVERR_BLOCK_ID);
-                                blk = 0;
-                            }
-                            const int64_t grow = ((int64_t)blk * p.Hkv + U.g) * p.bs + (valid ? pos % p.bs : 0);
-                            cp_async_16_zfill(dbase + (c >> 3) * C::kChunkBytes + sw128(row, c & 7),
-                                              src_base + grow * D + c * 8, valid);
-                        }
-                        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(full)) : "memory");
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(full);
-                    }
-                    if (which) last_v[st] = n + 1;
-                    else last_k[st] = n + 1;
+                uint64_t* full = which ? &v_full[st] : &k_full[st];
+                uint64_t* empty = which ? &v_empty[st] : &k_empty[st];
+                if (n > 0 && !mbar_wait(empty, (n - 1) & 1, p.err)) {
+                    s_abort = 1;
+                    ok = false;
+                    continue;
                 }
+                uint8_t* dst = smem + (which ? C::kOffV : C::kOffK) + st * C::kKVBytes;
+                if (U.slot == 0) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full, C::kKVBytes);
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(dst + c * C::kChunkBytes, which ? &maps.vnew : &maps.knew, full, c * 64, U.g,
+                                        U.q0 + kb, pol_kv);
+                    }
+                } else if (ctx_tma) {
+                    // one lane per block issues that block's boxes (in parallel)
+                    const int bs = p.bs;
+                    const int nvalid = min(BN / bs, (U.c1 - kb + bs - 1) / bs);
+                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nvalid * C::kChunks * bs * 128));
+                    __syncwarp();
+                    if (lane < nvalid) {
+                        const int row = (blk_mine * p.Hkv + U.g) * bs;
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_2d(dst + c * C::kChunkBytes + lane * bs * 128, which ? &maps.vc : &maps.kc, full,
+                                        c * 64, row, pol_kv);
+                    }
+                } else {
+                    // small blocks: 16-byte copies, rows past the chunk end zero-filled
+                    const uint32_t dbase = smem_u32(dst);
+                    const __nv_bfloat16* src_base = which ? p.v_cache : p.k_cache;
+                    for (int ci = lane; ci < BN * (D / 8); ci += 32) {
+                        const int row = ci / (D / 8), c = ci % (D / 8);
+                        const int pos = kb + row;
+                        const bool valid = pos < U.c1;
+                        int blk = valid ? __ldg(bt + pos / p.bs) : 0;
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            set_error(p.err, PKA_DEVERR_BLOCK_ID);
+                            blk = 0;
+                        }
+                        const int64_t grow = ((int64_t)blk * p.Hkv + U.g) * p.bs + (valid ? pos % p.bs : 0);
+                        cp_async_16_zfill(dbase + (c >> 3) * C::kChunkBytes + sw128(row, c & 7),
+                                          src_base + grow * D + c * 8, valid);
+                    }
+                    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(full)) : "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full);
+                }
+                if (which) last_v[st] = n + 1;
+                else last_k[st] = n + 1;
             }
             if (!ok) break;
         }
@@ -255,15 +260,17 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         }
         if (which == 0)
             for (uint32_t k = q_it > 2 ? q_it - 2 : 0; k < q_it; ++k) mbar_wait(&q_full[k & 1], (k >> 1) & 1, p.err);
-    } else if (warp == 1 || warp == 7) {
+    } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------------------ MMA issuers
-        // warp 1 streams S = Q K^T ahead of the softmax (gated only by a free S
-        // buffer and the K tile); warp 7 issues O += P V as each P lands. Each
-        // thread commits only its own MMAs.
+        // warp 1 issues S_k = Q K^T for tile t (k = t % 2) once the K tile is
+        // in and the previous P_k . V (which read P_k out of S_k's columns)
+        // is done; warp 3 issues O_k += P_k V as each P_k lands. Each thread
+        // commits only its own MMAs.
         if (lane == 0 && warp == 1) {
             constexpr uint32_t idesc_qk = umma_idesc_bf16(128, 128, 0, 0);
             const uint32_t q_s = sm_base + C::kOffQ, k_s = sm_base + C::kOffK;
-            uint32_t kv_it = 0, s_it = 0, q_it = 0;
+            uint32_t kv_it = 0, q_it = 0;
+            uint32_t nq[2] = {0, 0};  // products issued into S_k
             bool ok = true;
             FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
             for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x, ++q_it) {
@@ -276,29 +283,31 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 }
                 for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
                     const int st = kv_it & 1;
-                    const int b = s_it & 1;
+                    const int k = t & 1;
                     if (!mbar_wait(&k_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
-                    if (s_it >= 2 && !mbar_wait(&s_free[b], ((s_it >> 1) - 1) & 1, p.err)) { ok = false; break; }
+                    if (nq[k] > 0 && !mbar_wait(&pv_done[k], (nq[k] - 1) & 1, p.err)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-                        umma_bf16(tbase + C::kColS + b * 128, umma_desc_sw128(q_s + qb * C::kQBytes + off, 16, 1024),
+                        umma_bf16(tbase + C::kColS + k * 128, umma_desc_sw128(q_s + qb * C::kQBytes + off, 16, 1024),
                                   umma_desc_sw128(k_s + st * C::kKVBytes + off, 16, 1024), idesc_qk,
                                   ks > 0 ? 1u : 0u);
                     }
-                    umma_commit(&s_full[b]);
+                    umma_commit(&s_full[k]);
                     umma_commit(&k_empty[st]);
                     if (t == U.ntiles - 1) umma_commit(&q_empty[qb]);
-                    ++s_it;
+                    ++nq[k];
                 }
             }
             if (!ok) s_abort = 1;
-            if (s_it > 0) mbar_wait(&s_full[(s_it - 1) & 1], ((s_it - 1) >> 1) & 1, p.err);
-        } else if (lane == 0 && warp == 7) {
+            for (int k = 0; k < 2; ++k)
+                if (nq[k] > 0) mbar_wait(&s_full[k], (nq[k] - 1) & 1, p.err);
+        } else if (lane == 0 && warp == 3) {
             constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, 0, 1);
             const uint32_t v_s = sm_base + C::kOffV;
-            uint32_t kv_it = 0, pv_it = 0, q_it = 0;
+            uint32_t kv_it = 0, q_it = 0;
+            uint32_t np[2] = {0, 0};  // products issued from P_k
             bool ok = true;
             FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
             for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x, ++q_it) {
@@ -306,134 +315,128 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
                 for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
                     const int vs = kv_it & 1;
-                    const int pb = pv_it & 1;
-                    if (!mbar_wait(&p_full[pb], (pv_it >> 1) & 1, p.err)) { ok = false; break; }
+                    const int k = t & 1;
+                    if (!mbar_wait(&p_full[k], np[k] & 1, p.err)) { ok = false; break; }
                     if (!mbar_wait(&v_full[vs], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
-                    // the first product of a unit overwrites O: the previous unit's O must be read
+                    // a unit's first products overwrite O0 / O1: the previous epilogue must have read them
                     if (t == 0 && q_it > 0 && !mbar_wait(o_free, (q_it - 1) & 1, p.err)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
                         const uint64_t bdesc = umma_desc_sw128(v_s + vs * C::kKVBytes + kk * 2048, C::kChunkBytes, 1024);
-                        umma_bf16_ts(tbase + C::kColO, tbase + C::kColP + pb * 64 + kk * 8, bdesc, idesc_pv,
-                                     (t > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts(tbase + C::kColO + k * D, tbase + C::kColS + k * 128 + kk * 8, bdesc, idesc_pv,
+                                     (t >= 2 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(&pv_done[pb]);
+                    umma_commit(&pv_done[k]);
                     umma_commit(&v_empty[vs]);
-                    ++pv_it;
+                    ++np[k];
                 }
             }
             if (!ok) s_abort = 1;
             // let every issued MMA finish before the CTA can exit
-            if (pv_it > 0) mbar_wait(&pv_done[(pv_it - 1) & 1], ((pv_it - 1) >> 1) & 1, p.err);
+            for (int k = 0; k < 2; ++k)
+                if (np[k] > 0) mbar_wait(&pv_done[k], (np[k] - 1) & 1, p.err);
         }
-    } else {
-        // ------------------------------------------------------------ softmax warpgroup
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int k = warp >= 8 ? 1 : 0;
         const int row = 32 * (warp & 3) + lane;  // TMEM lane = query row of the tile
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        const int wg_tid = threadIdx.x - 64;
+        const int wg_tid = threadIdx.x - 128 * (k + 1);
+        const uint32_t tS = tbase + lane_off + C::kColS + k * 128;
+        const uint32_t tO = tbase + lane_off + C::kColO;  // O0; O1 follows after D columns
         const float sl2 = p.scale_log2;
-        uint32_t s_it = 0, kv_it = 0;
-        uint32_t p_it = 0;      // P buffers written (global)
-        uint32_t pv_seen = 0;   // P . V completions waited for (global, in order)
-        // wait until the P . V that used write number `k` (global) is done
-        auto wait_pv = [&](uint32_t k) -> bool {
-            while (pv_seen <= k) {
-                if (!mbar_wait(&pv_done[pv_seen & 1], (pv_seen >> 1) & 1, p.err)) return false;
-                ++pv_seen;
-            }
-            return true;
-        };
-        FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
-        for (int u = blockIdx.x; u < num_units && !s_abort; u += gridDim.x) {
-            const FaUnit U = Un;
-            if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
+        uint32_t n_s = 0;  // S tiles of this warpgroup (all units)
+        uint32_t kv_it = 0, q_it = 0;
+        for (int u = blockIdx.x; u < num_units && !s_abort; u += gridDim.x, ++q_it) {
+            const FaUnit U = fa_unit(p, u);  // the softmax waits for S anyway: no prefetch
             const int qi = U.row0 + row;  // query index within the request's new tokens
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
             const uint32_t kv_base = kv_it;
-            for (int t = 0; t < U.ntiles; ++t) {
-                const int b = s_it & 1;
-                if (!mbar_wait(&s_full[b], (s_it >> 1) & 1, p.err)) { ok = false; break; }
+            for (int t = k; t < U.ntiles; t += 2) {
+                if (!mbar_wait(&s_full[k], n_s & 1, p.err)) { ok = false; break; }
                 tc_fence_after();
-                float s[BN];
-                {
-                    uint32_t r0[32], r1[32], r2[32], r3[32];
-                    const uint32_t ta = tbase + lane_off + C::kColS + b * 128;
-                    tmem_ld32(ta, r0);
-                    tmem_ld32(ta + 32, r1);
-                    tmem_ld32(ta + 64, r2);
-                    tmem_ld32(ta + 96, r3);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        s[i] = __uint_as_float(r0[i]);
-                        s[32 + i] = __uint_as_float(r1[i]);
-                        s[64 + i] = __uint_as_float(r2[i]);
-                        s[96 + i] = __uint_as_float(r3[i]);
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_free[b]);
-                ++s_it;
-                // mask (raw scores), row max
                 const int kb = U.kb0 + t * BN;
                 const bool edge = (U.slot == 0) ? (kb + BN - 1 > U.row0 || kb + BN > U.c1)
                                                 : (kb < U.c0 || kb + BN > U.c1);
-                if (edge) {
-                    const int lo = U.c0 - kb;  // visible columns: [lo, hi)
-                    const int hi = ((U.slot == 0) ? min(qi + 1, U.c1) : U.c1) - kb;
-#pragma unroll
-                    for (int i = 0; i < BN; ++i) s[i] = (i >= lo && i < hi) ? s[i] : -INFINITY;
-                }
-                // row max as a tree over 8 independent chains
-                float mxv[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mxv[k] = s[k];
-#pragma unroll
-                for (int i = 8; i < BN; i += 8)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mxv[k] = fmaxf(mxv[k], s[i + k]);
-                const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
-                                       fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
-                const float m_new = fmaxf(m_used, mx * sl2);
+                const int lo = U.c0 - kb;  // visible columns: [lo, hi)
+                const int hi = ((U.slot == 0) ? min(qi + 1, U.c1) : U.c1) - kb;
+                // Pass 1: row max of the raw scores (8 independent chains). Pass 2:
+                // P = exp2(scale * s - m_used) as bf16 pairs, written over S_k's
+                // already-read columns (keys 32h.. land in columns 16h..). The body
+                // is specialised on whether the tile needs a mask at all (a
+                // per-element mask costs ALU issue slots on every tile otherwise).
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 bool rescale = false;
                 float alpha = 1.f;
-                if (t == 0) {
-                    m_used = m_new;
-                } else if (m_new > m_used + 8.f) {
-                    alpha = fast_exp2(m_used - m_new);
-                    rescale = true;
-                    l *= alpha;
-                    m_used = m_new;
-                }
-                // P = exp2(scale * s - m_used), kept packed in registers
-                uint32_t pk[BN / 2];
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                auto tile_body = [&](auto masked_c) {
+                    constexpr bool kMasked = decltype(masked_c)::value;
+                    float mxv[8];
 #pragma unroll
-                for (int i = 0; i < BN; i += 2) {
-                    const float e0 = fast_exp2(fmaf(s[i], sl2, -m_used));
-                    const float e1 = fast_exp2(fmaf(s[i + 1], sl2, -m_used));
-                    ls[(i >> 1) & 7] += e0 + e1;
-                    pk[i / 2] = pack_bf16(e0, e1);
-                }
-                l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                // O may be rescaled only once the previous P . V is done
-                if (rescale) {
-                    if (!wait_pv(p_it - 1)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int j = 0; j < 8; ++j) mxv[j] = -INFINITY;
+#pragma unroll 1
+                    for (int h = 0; h < 4; ++h) {
                         uint32_t r[32];
-                        tmem_ld32(tbase + lane_off + C::kColO + c * 32, r);
+                        tmem_ld32(tS + 32 * h, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tbase + lane_off + C::kColO + c * 32, r);
+                        for (int i = 0; i < 32; ++i) {
+                            float v = __uint_as_float(r[i]);
+                            if (kMasked && (unsigned)(32 * h + i - lo) >= (unsigned)(hi - lo)) v = -INFINITY;
+                            mxv[i & 7] = fmaxf(mxv[i & 7], v);
+                        }
                     }
-                    tmem_wait_st();
+                    const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                                           fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
+                    const float m_new = fmaxf(m_used, mx * sl2);
+                    if (t == k) {
+                        m_used = m_new;
+                    } else if (m_new > m_used + 8.f) {
+                        alpha = fast_exp2(m_used - m_new);
+                        rescale = true;
+                        l *= alpha;
+                        m_used = m_new;
+                    }
+                    const float m_off = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll 1
+                    for (int h = 0; h < 4; ++h) {
+                        uint32_t r[32];
+                        tmem_ld32(tS + 32 * h, r);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float v0 = __uint_as_float(r[i]);
+                            float v1 = __uint_as_float(r[i + 1]);
+                            if (kMasked) {
+                                if ((unsigned)(32 * h + i - lo) >= (unsigned)(hi - lo)) v0 = -INFINITY;
+                                if ((unsigned)(32 * h + i + 1 - lo) >= (unsigned)(hi - lo)) v1 = -INFINITY;
+                            }
+                            const float e0 = fast_exp2(fmaf(v0, sl2, -m_off));
+                            const float e1 = fast_exp2(fmaf(v1, sl2, -m_off));
+                            ls[(i >> 1) & 7] += e0 + e1;
+                            pk[i / 2] = pack_bf16(e0, e1);
+                        }
+                        tmem_st16(tS + 16 * h, pk);
+                    }
+                };
+                if (edge) tile_body(std::true_type{});
+                else tile_body(std::false_type{});
+                l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                // O_k's previous product finished before this S tile was computed
+                if (rescale) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 16; ++c) {
+                        uint32_t r[16];
+                        tmem_ld16(tO + k * D + c * 16, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st16(tO + k * D + c * 16, r);
+                    }
                 }
+                tmem_wait_st();
                 // last tile of a context chunk: value rows past the chunk end may
                 // hold anything (other positions, NaN-poisoned slots): zero them
                 if (U.slot != 0 && kb + BN > U.c1) {
@@ -446,75 +449,90 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                         *reinterpret_cast<uint4*>(vt + (c >> 3) * C::kChunkBytes + sw128(vr, c & 7)) =
                             make_uint4(0, 0, 0, 0);
                     }
-                }
-                // P buffer p_it & 1 (TMEM) was last read by P . V number p_it - 2
-                if (p_it >= 2 && !wait_pv(p_it - 2)) { ok = false; break; }
-                {
-                    const uint32_t pa = tbase + lane_off + C::kColP + (p_it & 1) * 64;
-                    uint32_t h0[32], h1[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        h0[i] = pk[i];
-                        h1[i] = pk[32 + i];
-                    }
-                    tmem_st32(pa, h0);
-                    tmem_st32(pa + 32, h1);
-                    tmem_wait_st();
+                    fence_proxy_async_smem();  // the tensor core reads these rows through the async proxy
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[p_it & 1]);
-                ++p_it;
+                if (lane == 0) mbar_arrive(&p_full[k]);
+                ++n_s;
             }
             kv_it = kv_base + U.ntiles;
             if (!ok) {
                 s_abort = 1;
                 break;
             }
-            // ---- epilogue: O row / l once the unit's last P . V is done
-            if (!wait_pv(p_it - 1)) {
+            // ---- epilogue: merge the two warpgroups' (max, sum, O) like two KV splits
+            const FaUnit E = fa_unit(p, u);  // re-read rather than kept live through the tile loop
+            const int n_mine = (E.ntiles - k + 1) / 2, n_other = (E.ntiles - (1 - k) + 1) / 2;
+            if (n_mine > 0 && !mbar_wait(&pv_done[k], (n_s - 1) & 1, p.err)) {
+                s_abort = 1;
+                break;
+            }
+            s_ml[q_it & 1][k][row] = make_float2(m_used, l);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ml_ready);
+            if (!mbar_wait(ml_ready, q_it & 1, p.err)) {
                 s_abort = 1;
                 break;
             }
             tc_fence_after();
-            float o[D];
-            {
-                uint32_t r[D / 32][32];
+            const float2 mo = s_ml[q_it & 1][1 - k][row];
+            const float m = fmaxf(m_used, mo.x);
+            const float f_me = n_mine > 0 ? fast_exp2(m_used - m) : 0.f;
+            const float f_ot = n_other > 0 ? fast_exp2(mo.x - m) : 0.f;
+            const float L = f_me * l + f_ot * mo.y;
+            const float inv = 1.f / L;
+            const float a_me = f_me * inv, a_ot = f_ot * inv;
+            const bool write = qi < E.qlen;
+            const bool final_out = E.slot == 0 && E.ctx == 0;
+            const int64_t orow = final_out ? ((int64_t)(E.q0 + qi) * p.Hq + E.h)
+                                           : (((int64_t)p.ext_base[E.r - p.num_decodes] + (int64_t)E.slot * E.qlen + qi) *
+                                                  p.Hq + E.h);
+            // this warpgroup writes columns [k D/2, (k+1) D/2) of the row: read and
+            // combine both accumulators' halves, release O, then store
+            constexpr int kHalf = D / 2;
+            float o[kHalf];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_ld32(tbase + lane_off + C::kColO + c * 32, r[c]);
+            for (int c = 0; c < kHalf / 32; ++c) {
+                const int col0 = k * kHalf + c * 32;
+                uint32_t ra[32], rb[32];
+                if (n_mine > 0) tmem_ld32(tO + k * D + col0, ra);
+                if (n_other > 0) tmem_ld32(tO + (1 - k) * D + col0, rb);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(r[c][i]);
+                for (int i = 0; i < 32; ++i)
+                    o[c * 32 + i] = (n_mine > 0 ? a_me * __uint_as_float(ra[i]) : 0.f) +
+                                    (n_other > 0 ? a_ot * __uint_as_float(rb[i]) : 0.f);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
-            if (qi < U.qlen) {
-                const float inv = 1.f / l;
-                const float lse_nat = (m_used + __log2f(l)) * 0.69314718055994531f;
-                if (U.slot == 0 && U.ctx == 0) {
-                    __nv_bfloat16* dst = p.out + ((int64_t)(U.q0 + qi) * p.Hq + U.h) * D;
+            if (write) {
+                if (final_out) {
+                    __nv_bfloat16* dst = p.out + orow * D + k * kHalf;
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
+                    for (int j = 0; j < kHalf / 8; ++j) {
                         uint4 v;
-                        v.x = pack_bf16(o[c * 8 + 0] * inv, o[c * 8 + 1] * inv);
-                        v.y = pack_bf16(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv);
-                        v.z = pack_bf16(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv);
-                        v.w = pack_bf16(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv);
-                        *reinterpret_cast<uint4*>(dst + c * 8) = v;
+                        v.x = pack_bf16(o[j * 8 + 0], o[j * 8 + 1]);
+                        v.y = pack_bf16(o[j * 8 + 2], o[j * 8 + 3]);
+                        v.z = pack_bf16(o[j * 8 + 4], o[j * 8 + 5]);
+                        v.w = pack_bf16(o[j * 8 + 6], o[j * 8 + 7]);
+                        *reinterpret_cast<uint4*>(dst + j * 8) = v;
                     }
-                    if (p.lse) p.lse[(int64_t)(U.q0 + qi) * p.Hq + U.h] = lse_nat;
                 } else {
-                    const int64_t prow =
-                        ((int64_t)p.ext_base[U.r - p.num_decodes] + (int64_t)U.slot * U.qlen + qi) * p.Hq + U.h;
-                    float* dst = p.ext_o + prow * D;
+                    float* dst = p.ext_o + orow * D + k * kHalf;
 #pragma unroll
-                    for (int c = 0; c < D / 4; ++c)
-                        *reinterpret_cast<float4*>(dst + c * 4) =
-                            make_float4(o[c * 4] * inv, o[c * 4 + 1] * inv, o[c * 4 + 2] * inv, o[c * 4 + 3] * inv);
-                    p.ext_lse[prow] = lse_nat;
+                    for (int j = 0; j < kHalf / 4; ++j)
+                        *reinterpret_cast<float4*>(dst + j * 4) = make_float4(o[j * 4], o[j * 4 + 1], o[j * 4 + 2], o[j * 4 + 3]);
+                }
+            }
+            if (write && k == 0) {
+                const float lse_nat = (m + __log2f(L)) * 0.69314718055994531f;
+                if (final_out) {
+                    if (p.lse) p.lse[orow] = lse_nat;
+                } else {
+                    p.ext_lse[orow] = lse_nat;
                 }
             }
         }

@@ -86,6 +86,8 @@ def _fwd(lib, **kw):
     (dict(T=3), 1),                        # fewer tokens than the batch needs
     (dict(maxb=2), 1),                     # table narrower than max_seq_len needs
     (dict(scale=float("inf")), 1),
+    (dict(scale=0.0), 1),                  # the row max and the masking assume scale > 0
+    (dict(scale=-0.125), 1),
     (dict(ws=P(0x100010)), 1),             # workspace not 256-byte aligned
     (dict(v_cache=None), 2),               # latent cache with d = 64
     (dict(v_cache=None, d=576, dv=512, Hq=128, Hkv=1), 2),  # latent cache: decode only
