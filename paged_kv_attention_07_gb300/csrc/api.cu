@@ -31,8 +31,15 @@ cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bou
                                  cudaStream_t stream);
 int decode_gqa_target_units(int num_sms);
 int decode_mla_heads_per_cta(int Hq);
+bool decode_mla_tc_supported(int Hq);
+cudaError_t launch_decode_mla_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecodeMlaParams& p,
+                                 int num_sms, cudaStream_t stream);
 
-static int mla_units_per_pair(int Hq) { return Hq / decode_mla_heads_per_cta(Hq); }
+// MLA decode units per (request, split): on the tensor-core kernel two value
+// halves per group of 128 heads, otherwise one unit per 64-head group.
+static int mla_units_per_pair(int Hq) {
+    return decode_mla_tc_supported(Hq) ? 2 * (Hq / 128) : Hq / decode_mla_heads_per_cta(Hq);
+}
 
 namespace {
 
@@ -81,6 +88,21 @@ bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 view of a token-major tensor [T, H, D] read in boxes of 64
+// columns x `box_heads` heads x 1 token (128-byte swizzle): one box gives 64
+// dims of a run of consecutive heads of one token.
+bool encode_heads(CUtensorMap* map, const void* base, uint64_t T, uint64_t H, uint64_t D, uint32_t box_heads) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {D, H, T};
+    cuuint64_t strides[2] = {D * 2, H * D * 2};
+    cuuint32_t box[3] = {64, box_heads, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -351,7 +373,8 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
     pp.dec_units_per_pair = is_mla ? mla_units_per_pair(num_q_heads) : num_kv_heads;
     pp.dec_target_units = L.dec_target_units;
     pp.dec_min_split = is_mla ? kMlaMinSplit : kDecodeMinSplit;
-    pp.dec_split_align = 16;
+    // the tensor-core MLA kernel reads 64-key tiles whose TMA boxes must start on block rows
+    pp.dec_split_align = (is_mla && decode_mla_tc_supported(num_q_heads)) ? 64 : 16;
     pp.dec_pair_cap = L.dec_pair_cap;
     pp.fa_item_cap = L.fa_item_cap;
     pp.ext_row_cap = L.ext_row_cap;
@@ -373,9 +396,14 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
     if (num_decodes > 0) {
         const bool tma = block_size >= 8;
         if (is_mla) {
-            CUtensorMap map;
+            const bool tc = decode_mla_tc_supported(num_q_heads);
+            CUtensorMap map, qmap;
             std::memset(&map, 0, sizeof(map));
-            if (tma && !encode_rows(&map, k_cache, (uint64_t)cache_rows, 576, (uint32_t)std::min(block_size, 16)))
+            std::memset(&qmap, 0, sizeof(qmap));
+            if (tma && !encode_rows(&map, k_cache, (uint64_t)cache_rows, 576,
+                                    (uint32_t)std::min(block_size, tc ? 64 : 16)))
+                return PKA_ERR_CUDA;
+            if (tc && !encode_heads(&qmap, q, (uint64_t)num_tokens, (uint64_t)num_q_heads, 576, 128))
                 return PKA_ERR_CUDA;
             DecodeMlaParams dp;
             dp.q = static_cast<const __nv_bfloat16*>(q);
@@ -395,10 +423,11 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
             dp.max_blocks = max_blocks_per_req;
             dp.Hq = num_q_heads;
             dp.bs = block_size;
-            dp.groups = num_q_heads / decode_mla_heads_per_cta(num_q_heads);
+            dp.groups = tc ? num_q_heads / 128 : num_q_heads / decode_mla_heads_per_cta(num_q_heads);
             dp.scale_log2 = scale_log2;
-            if ((e = timed(PKA_KERNEL_DECODE, st, [&] { return launch_decode_mla(map, dp, tma, sms, st); })) !=
-                cudaSuccess)
+            if ((e = timed(PKA_KERNEL_DECODE, st, [&] {
+                     return tc ? launch_decode_mla_tc(map, qmap, dp, sms, st) : launch_decode_mla(map, dp, tma, sms, st);
+                 })) != cudaSuccess)
                 return PKA_ERR_CUDA;
         } else {
             CUtensorMap km, vm;
@@ -612,7 +641,8 @@ pka_status pka_paged_decode_noalloc(const void* q, const void* k_cache, const vo
     pp.dec_units_per_pair = num_kv_heads;
     pp.dec_target_units = (int)target;
     pp.dec_min_split = kDecodeMinSplit;
-    pp.dec_split_align = 16;
+    // the tensor-core MLA kernel reads 64-key tiles whose TMA boxes must start on block rows
+    pp.dec_split_align = (is_mla && decode_mla_tc_supported(num_q_heads)) ? 64 : 16;
     pp.dec_pair_cap = pair_cap;
     pp.hdr = hdr;
     pp.dec_pairs = reinterpret_cast<int2*>(ws + off_pairs);

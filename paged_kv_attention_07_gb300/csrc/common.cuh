@@ -93,6 +93,15 @@ PKA_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
     }
 }
 
+// Full-warp forms: every lane of the warp gets the same answer, so a timeout
+// or an abort can never split a warp at a later warp-synchronous point
+// (__syncwarp, shuffles, .sync.aligned instructions). Call with all 32 lanes.
+PKA_DEVICE bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int32_t* err) {
+    const bool ok = mbar_wait(bar, parity, err);
+    return __all_sync(0xffffffffu, ok);
+}
+PKA_DEVICE bool warp_flag(const volatile int& flag) { return __any_sync(0xffffffffu, flag != 0); }
+
 // Generic-proxy accesses to shared memory made before this fence are ordered
 // before later async-proxy (TMA / tensor core) accesses.
 PKA_DEVICE void fence_proxy_async_smem() {

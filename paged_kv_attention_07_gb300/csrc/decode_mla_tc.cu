@@ -1,0 +1,505 @@
+// decode_mla_tc.cu -- absorbed MLA decode on the 5th-generation tensor cores
+// ("vLLM AMD ROCm Attention Backends Optimization", section "The hybrid
+// processing strategy": decode works directly on the compressed 576-dim
+// latent; the value is the latent's first 512 dims), for groups of 128
+// query heads.
+//
+// Per key j one latent row c_j serves every head:
+//     s_hj = scale * <q_h, c_j[0:576]>,   o_h = sum_j softmax_j(s_h) c_j[0:512].
+// The 128 heads are the MMA's M (one TMEM lane each). Their fp32 output
+// (128 x 512) alone would fill a whole SM's tensor memory, so a work unit is
+// (request split, head group, value half): the two halves of a split run on
+// two CTAs that compute the same scores (identical arithmetic, so identical
+// softmax statistics) and each accumulate 256 value dims. They are adjacent
+// in the unit order, so the second read of every latent tile hits L2.
+//
+// Tensor memory (512 columns, lane = head):
+//     [0, 64)    S   fp32 scores of a 64-key tile
+//     [64, 96)   P   bf16 pairs, the A operand of O += P . V
+//     [96, 256)  Qt  bf16 pairs of q[:, 0:320], the A operand of the first
+//                    20 k-steps of S (no shared-memory traffic for them)
+//     [256, 512) O   fp32, this unit's 256 value dims
+// Shared memory: q[:, 320:576] (64 KB, the A operand of the last 16 k-steps)
+// and a 2-stage ring of 64-key latent tiles (72 KB each), loaded with TMA
+// boxes of 64 dims x min(block size, 64) rows walked through the block table
+// (16-byte cp.async copies below block size 8 and for a split's last,
+// partial tile, whose missing rows are zero-filled).
+//
+// Persistent CTAs, one per SM, allocate tensor memory once and take units
+// from an atomic counter; the producer publishes each unit index to the other
+// roles through a 2-slot ring in shared memory. Warps: 0 producer, 1 tensor-
+// memory owner + MMA issuer (one thread), 2-5 softmax (one thread per head):
+// S row -> online softmax (the O rescale is lazy: only when the max grew by
+// more than 2^8) -> P into TMEM; at the end of a unit O / l goes to out, or
+// to the fp32 split partials + LSE that the decode reduction merges.
+#include "common.cuh"
+#include "params.cuh"
+#include "plan.cuh"
+#include "tcgen05.cuh"
+
+namespace pka {
+
+constexpr int kMtThreads = 192;
+constexpr int kMtTile = 64;                       // keys per tile (the N of S)
+constexpr int kMtD = 576, kMtDv = 512, kMtHalf = 256;
+constexpr int kMtQtDims = 320;                    // q dims held in TMEM
+constexpr int kMtChunk = kMtTile * 128;           // one 64-dim column chunk of a tile (8 KB)
+constexpr int kMtTileBytes = 9 * kMtChunk;        // 72 KB
+constexpr int kMtQsChunk = 128 * 128;             // 128 heads x 64 dims
+constexpr int kMtQsBytes = 4 * kMtQsChunk;        // q[:, 320:576]
+constexpr int kMtOffQ = 0;
+constexpr int kMtOffKV = kMtQsBytes;
+constexpr int kMtOffBar = kMtOffKV + 2 * kMtTileBytes;
+constexpr int kMtSmem = kMtOffBar + 256 + 1024;
+constexpr uint32_t kMtColS = 0, kMtColP = 64, kMtColQ = 96, kMtColO = 256, kMtCols = 512;
+
+struct MlaTcUnit {
+    int pair, grp, half, r, k0, k1, ntiles;
+};
+
+PKA_DEVICE MlaTcUnit mla_tc_unit(const DecodeMlaParams& p, int u, int L) {
+    MlaTcUnit U;
+    const int upp = 2 * p.groups;
+    U.pair = u / upp;
+    const int rem = u - U.pair * upp;
+    U.grp = rem >> 1;
+    U.half = rem & 1;
+    const int2 rs = p.pairs[U.pair];
+    U.r = rs.x;
+    U.k0 = rs.y * L;
+    U.k1 = min(U.k0 + L, p.seq_lens[U.r]);
+    U.ntiles = (U.k1 - U.k0 + kMtTile - 1) / kMtTile;
+    return U;
+}
+
+// A unit the kernel can run without touching memory it does not own.
+PKA_DEVICE bool mla_tc_unit_ok(const DecodeMlaParams& p, const MlaTcUnit& U) {
+    return U.r >= 0 && U.k0 >= 0 && U.k1 > U.k0 && U.grp < p.groups;
+}
+
+__global__ void __launch_bounds__(kMtThreads, 1)
+    decode_mla_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap,
+                         const DecodeMlaParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMtOffBar);
+    uint64_t* kv_full = bars + 0;    // [2] per latent stage
+    uint64_t* kv_empty = bars + 2;   // [2]
+    uint64_t* u_full = bars + 4;     // [2] unit ring slot written
+    uint64_t* u_empty = bars + 6;    // [2] unit ring slot read by the issuer and the 4 softmax warps
+    uint64_t* q_full = bars + 8;     // q[:, 320:576] landed in shared memory
+    uint64_t* q_empty = bars + 9;    // the unit's last S product is done (Q free again)
+    uint64_t* qt_ready = bars + 10;  // q[:, 0:320] written to TMEM (4 warps)
+    uint64_t* s_full = bars + 11;
+    uint64_t* s_free = bars + 12;    // 4 warps read S
+    uint64_t* p_full = bars + 13;    // 4 warps wrote P (and rescaled O)
+    uint64_t* pv_done = bars + 14;
+    uint64_t* o_free = bars + 15;    // 4 warps read O
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_unit[2];
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_units = p.hdr->dec_num_pairs * 2 * p.groups;
+    if (num_units == 0) return;
+    const int L = p.hdr->dec_split_len;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&u_full[i], 1);
+            mbar_init(&u_empty[i], 5);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        mbar_init(qt_ready, 4);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 4);
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(o_free, 4);
+        fence_barrier_init();
+        s_abort = 0;
+        tma_prefetch_desc(&kvmap);
+        tma_prefetch_desc(&qmap);
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, kMtCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = s_tmem;
+    const uint32_t sm_base = smem_u32(smem);
+
+    // Next unit index from the ring (every consumer reads each slot once).
+    auto take_unit = [&](uint32_t i, bool arrive, int* u) -> bool {
+        const int slot = i & 1;
+        if (!mbar_wait_warp(&u_full[slot], (i >> 1) & 1, p.err)) return false;
+        *u = s_unit[slot];
+        __syncwarp();
+        if (arrive) mbar_arrive(&u_empty[slot]);
+        return true;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = policy_evict_normal();  // the other value half re-reads each tile
+        const bool use_tma = p.bs >= 8;
+        uint32_t kv_it = 0, q_it = 0;
+        uint32_t last[2] = {0, 0};  // phase + 1 of the last copy per stage (0 = none)
+        for (uint32_t i = 0; !warp_flag(s_abort); ++i) {
+            const int slot = i & 1;
+            if (i >= 2 && !mbar_wait_warp(&u_empty[slot], ((i >> 1) - 1) & 1, p.err)) {
+                s_abort = 1;
+                break;
+            }
+            int u = 0;
+            if (lane == 0) u = atomicAdd(p.counter, 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (u >= num_units) u = -1;
+            if (lane == 0) {
+                s_unit[slot] = u;
+                mbar_arrive(&u_full[slot]);
+            }
+            __syncwarp();
+            if (u < 0) break;
+            const MlaTcUnit U = mla_tc_unit(p, u, L);
+            if (!mla_tc_unit_ok(p, U)) {
+                if (lane == 0) set_error(p.err, PKA_DEVERR_CAPACITY);
+                continue;
+            }
+            if (q_it > 0 && !mbar_wait_warp(q_empty, (q_it - 1) & 1, p.err)) {
+                s_abort = 1;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(q_full, kMtQsBytes);
+                for (int c = 0; c < 4; ++c)
+                    tma_load_3d(smem + kMtOffQ + c * kMtQsChunk, &qmap, q_full, kMtQtDims + c * 64, U.grp * 128, U.r,
+                                pol);
+            }
+            ++q_it;
+            const int32_t* bt = p.block_table + (int64_t)U.r * p.max_blocks;
+            bool ok = true;
+            for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
+                const int st = kv_it & 1;
+                const uint32_t n = kv_it >> 1;
+                if (n > 0 && !mbar_wait_warp(&kv_empty[st], (n - 1) & 1, p.err)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* dst = smem + kMtOffKV + st * kMtTileBytes;
+                const int tb = U.k0 + t * kMtTile;
+                const int valid = min(kMtTile, U.k1 - tb);
+                if (use_tma && valid == kMtTile) {
+                    const int rows = p.bs < kMtTile ? p.bs : kMtTile;  // rows per box
+                    const int nbox = kMtTile / rows;
+                    if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], kMtTileBytes);
+                    __syncwarp();
+                    if (lane < nbox) {  // one lane per box, in parallel
+                        const int pos = tb + lane * rows;
+                        int blk = __ldg(bt + pos / p.bs);
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            set_error(p.err, PKA_DEVERR_BLOCK_ID);
+                            blk = 0;
+                        }
+                        const int row = blk * p.bs + (pos % p.bs);
+                        for (int c = 0; c < 9; ++c)
+                            tma_load_2d(dst + c * kMtChunk + lane * rows * 128, &kvmap, &kv_full[st], c * 64, row, pol);
+                    }
+                } else {
+                    // 16-byte copies; rows past the split's end are zero-filled
+                    // (no NaN from slots the batch does not own)
+                    const uint32_t dbase = smem_u32(dst);
+                    for (int ci = lane; ci < kMtTile * (kMtD / 8); ci += 32) {
+                        const int tr = ci / (kMtD / 8), c = ci % (kMtD / 8);
+                        const int pos = tb + tr;
+                        const bool in = pos < U.k1;
+                        int blk = in ? __ldg(bt + pos / p.bs) : 0;
+                        if (blk < 0 || blk >= p.num_blocks) {
+                            set_error(p.err, PKA_DEVERR_BLOCK_ID);
+                            blk = 0;
+                        }
+                        const int64_t row = (int64_t)blk * p.bs + (in ? pos % p.bs : 0);
+                        cp_async_16_zfill(dbase + (c >> 3) * kMtChunk + sw128(tr, c & 7), p.kv + row * kMtD + c * 8, in);
+                    }
+                    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
+                                 : "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&kv_full[st]);
+                }
+                last[st] = n + 1;
+            }
+            if (!ok) {
+                s_abort = 1;
+                break;
+            }
+        }
+        // no copy may outlive the CTA: wait (bounded) for the last one per stage
+        for (int st = 0; st < 2; ++st)
+            if (last[st]) mbar_wait_warp(&kv_full[st], (last[st] - 1) & 1, p.err);
+        if (q_it > 0) mbar_wait_warp(q_full, (q_it - 1) & 1, p.err);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc_s = umma_idesc_bf16(128, kMtTile, 0, 0);
+        constexpr uint32_t idesc_o = umma_idesc_bf16(128, kMtHalf, 0, 1);
+        const uint32_t q_s = sm_base + kMtOffQ, kv_s = sm_base + kMtOffKV;
+        uint32_t kv_it = 0, s_it = 0, pv_it = 0, q_it = 0;
+        bool ok = true;
+        // S = q . C^T over all 576 dims: 20 k-steps with A (q[:, 0:320]) in
+        // TMEM, 16 with A (q[:, 320:576]) in shared memory
+        auto issue_s = [&](uint32_t kvi) {
+            const uint32_t kv = kv_s + (kvi & 1) * kMtTileBytes;
+#pragma unroll
+            for (int ks = 0; ks < kMtQtDims / 16; ++ks)
+                umma_bf16_ts(tbase + kMtColS, tbase + kMtColQ + ks * 8,
+                             umma_desc_sw128(kv + (ks >> 2) * kMtChunk + (ks & 3) * 32, 16, 1024), idesc_s,
+                             ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = kMtQtDims / 16; ks < kMtD / 16; ++ks) {
+                const int kq = ks - kMtQtDims / 16;
+                umma_bf16(tbase + kMtColS, umma_desc_sw128(q_s + (kq >> 2) * kMtQsChunk + (kq & 3) * 32, 16, 1024),
+                          umma_desc_sw128(kv + (ks >> 2) * kMtChunk + (ks & 3) * 32, 16, 1024), idesc_s, 1u);
+            }
+            umma_commit(s_full);
+        };
+        // O(half) += P . C[:, half*256 .. +256)
+        auto issue_o = [&](uint32_t kvi, int half, bool first) -> bool {
+            if (!mbar_wait(p_full, pv_it & 1, p.err)) return false;
+            // a unit's first product overwrites O: the previous unit's O must have been read
+            if (first && q_it > 1 && !mbar_wait(o_free, (q_it - 2) & 1, p.err)) return false;
+            tc_fence_after();
+            const uint32_t v = kv_s + (kvi & 1) * kMtTileBytes + half * 4 * kMtChunk;
+#pragma unroll
+            for (int kk = 0; kk < kMtTile / 16; ++kk)
+                umma_bf16_ts(tbase + kMtColO, tbase + kMtColP + kk * 8, umma_desc_sw128(v + kk * 16 * 128, kMtChunk, 1024),
+                             idesc_o, (!first || kk > 0) ? 1u : 0u);
+            umma_commit(pv_done);
+            umma_commit(&kv_empty[kvi & 1]);
+            ++pv_it;
+            return true;
+        };
+        for (uint32_t i = 0; ok && !warp_flag(s_abort); ++i) {
+            int u = 0;
+            if (!take_unit(i, lane == 0, &u)) {
+                ok = false;
+                break;
+            }
+            if (u < 0) break;
+            const MlaTcUnit U = mla_tc_unit(p, u, L);
+            if (!mla_tc_unit_ok(p, U)) continue;
+            ++q_it;  // units started (1-based below)
+            if (lane == 0) {
+                if (!mbar_wait(q_full, (q_it - 1) & 1, p.err) || !mbar_wait(qt_ready, (q_it - 1) & 1, p.err)) {
+                    ok = false;
+                } else {
+                    const uint32_t kv_base = kv_it;
+                    for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
+                        if (!mbar_wait(&kv_full[kv_it & 1], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                        if (s_it > 0 && !mbar_wait(s_free, (s_it - 1) & 1, p.err)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_s(kv_it);
+                        ++s_it;
+                        if (t == U.ntiles - 1) umma_commit(q_empty);
+                        if (t > 0 && !issue_o(kv_it - 1, U.half, t == 1)) { ok = false; break; }
+                    }
+                    if (ok && !issue_o(kv_base + U.ntiles - 1, U.half, U.ntiles == 1)) ok = false;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            kv_it = __shfl_sync(0xffffffffu, kv_it, 0);
+        }
+        if (!ok) s_abort = 1;
+        // let every issued MMA finish before the CTA can exit
+        if (lane == 0 && pv_it > 0) mbar_wait(pv_done, (pv_it - 1) & 1, p.err);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax (one thread per head)
+        const int hl = 32 * (warp & 3) + lane;  // head within the group = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tS = tbase + lane_off + kMtColS, tP = tbase + lane_off + kMtColP;
+        const uint32_t tQ = tbase + lane_off + kMtColQ, tO = tbase + lane_off + kMtColO;
+        const float sl2 = p.scale_log2;
+        uint32_t s_it = 0, pv_seen = 0;
+        for (uint32_t i = 0; !warp_flag(s_abort); ++i) {
+            int u = 0;
+            if (!take_unit(i, lane == 0, &u)) {
+                s_abort = 1;
+                break;
+            }
+            if (u < 0) break;
+            const MlaTcUnit U = mla_tc_unit(p, u, L);
+            if (!mla_tc_unit_ok(p, U)) continue;
+            const int h = U.grp * 128 + hl;
+            // q[h, 0:320] -> TMEM. The previous unit's last S product, the
+            // only reader of these columns, is done: this warp saw its S.
+            {
+                const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)U.r * p.Hq + h) * kMtD);
+#pragma unroll 1
+                for (int c = 0; c < kMtQtDims / 64; ++c) {  // 64 dims = 32 columns per step
+                    uint32_t r[32];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint4 v = __ldg(qrow + c * 8 + k);
+                        r[4 * k] = v.x;
+                        r[4 * k + 1] = v.y;
+                        r[4 * k + 2] = v.z;
+                        r[4 * k + 3] = v.w;
+                    }
+                    tmem_st32(tQ + c * 32, r);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qt_ready);
+            }
+            float m_used = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int t = 0; t < U.ntiles; ++t) {
+                if (!mbar_wait_warp(s_full, s_it & 1, p.err)) { ok = false; break; }
+                tc_fence_after();
+                float s[kMtTile];
+                {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tS, r0);
+                    tmem_ld32(tS + 32, r1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        s[k] = __uint_as_float(r0[k]);
+                        s[32 + k] = __uint_as_float(r1[k]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);
+                ++s_it;
+                const int valid = min(kMtTile, U.k1 - (U.k0 + t * kMtTile));
+                if (valid < kMtTile) {
+#pragma unroll
+                    for (int k = 0; k < kMtTile; ++k) s[k] = k < valid ? s[k] : -INFINITY;
+                }
+                float mv[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mv[k] = s[k];
+#pragma unroll
+                for (int k = 8; k < kMtTile; k += 8)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) mv[j] = fmaxf(mv[j], s[k + j]);
+                const float mx = fmaxf(fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])),
+                                       fmaxf(fmaxf(mv[4], mv[5]), fmaxf(mv[6], mv[7])));
+                const float m_new = fmaxf(m_used, mx * sl2);
+                bool rescale = false;
+                float alpha = 1.f;
+                if (t == 0) {
+                    m_used = m_new;
+                } else if (m_new > m_used + 8.f) {
+                    alpha = fast_exp2(m_used - m_new);
+                    rescale = true;
+                    l *= alpha;
+                    m_used = m_new;
+                }
+                uint32_t pk[kMtTile / 2];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < kMtTile; k += 2) {
+                    const float e0 = fast_exp2(fmaf(s[k], sl2, -m_used));
+                    const float e1 = fast_exp2(fmaf(s[k + 1], sl2, -m_used));
+                    ls[(k >> 1) & 3] += e0 + e1;
+                    pk[k / 2] = pack_bf16(e0, e1);
+                }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                // the previous P . V must be done before P or O change
+                if (t > 0) {
+                    if (!mbar_wait_warp(pv_done, pv_seen & 1, p.err)) { ok = false; break; }
+                    ++pv_seen;
+                    tc_fence_after();
+                }
+                // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
+                // takes this branch if any of its heads needs the rescale (alpha
+                // stays 1 for the others)
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                    for (int c = 0; c < kMtHalf / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+                        tmem_st32(tO + c * 32, r);
+                    }
+                }
+                tmem_st32(tP, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
+            }
+            if (!ok) {
+                s_abort = 1;
+                break;
+            }
+            if (!mbar_wait_warp(pv_done, pv_seen & 1, p.err)) {
+                s_abort = 1;
+                break;
+            }
+            ++pv_seen;
+            tc_fence_after();
+            // ---- epilogue: this half's 256 value dims of O / l
+            const bool direct = p.nsplit[U.r] == 1;
+            const float inv = 1.f / l;
+            const int64_t orow = direct ? ((int64_t)U.r * p.Hq + h) : ((int64_t)U.pair * p.Hq + h);
+#pragma unroll 1
+            for (int c = 0; c < kMtHalf / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tO + c * 32, r);
+                tmem_wait_ld();
+                const int d0 = U.half * kMtHalf + c * 32;
+                if (direct) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kMtDv + d0);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(pack_bf16(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
+                                            pack_bf16(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
+                                            pack_bf16(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
+                                            pack_bf16(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.part_o + orow * kMtDv + d0);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
+                                             __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
+            if (U.half == 0) {
+                const float lse_nat = (m_used + __log2f(l)) * 0.69314718055994531f;
+                if (direct) {
+                    if (p.lse) p.lse[orow] = lse_nat;
+                } else {
+                    p.part_lse[orow] = lse_nat;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kMtCols);
+    }
+}
+
+bool decode_mla_tc_supported(int Hq) { return Hq > 0 && Hq % 128 == 0; }
+
+cudaError_t launch_decode_mla_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecodeMlaParams& p,
+                                 int num_sms, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(decode_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMtSmem);
+    if (e != cudaSuccess) return e;
+    decode_mla_tc_kernel<<<num_sms, kMtThreads, kMtSmem, stream>>>(kvmap, qmap, p);
+    return cudaGetLastError();
+}
+
+}  // namespace pka

@@ -176,11 +176,11 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         uint32_t kv_it = 0, q_it = 0;
         uint32_t last_k[2] = {0, 0}, last_v[2] = {0, 0};  // phase + 1 of the last copy per stage (0 = none)
         FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
-        for (int u = blockIdx.x; u < num_units && !s_abort; u += gridDim.x, ++q_it) {
+        for (int u = blockIdx.x; u < num_units && !warp_flag(s_abort); u += gridDim.x, ++q_it) {
             const FaUnit U = Un;
             if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);  // prefetch
             const int qb = q_it & 1;
-            if (which == 0 && q_it >= 2 && !mbar_wait(&q_empty[qb], ((q_it >> 1) - 1) & 1, p.err)) {
+            if (which == 0 && q_it >= 2 && !mbar_wait_warp(&q_empty[qb], ((q_it >> 1) - 1) & 1, p.err)) {
                 s_abort = 1;
                 break;
             }
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 if (paged_tma && t + 1 < U.ntiles) blk_next = tile_block_id(p, bt, kb + BN, U.c1, lane);
                 uint64_t* full = which ? &v_full[st] : &k_full[st];
                 uint64_t* empty = which ? &v_empty[st] : &k_empty[st];
-                if (n > 0 && !mbar_wait(empty, (n - 1) & 1, p.err)) {
+                if (n > 0 && !mbar_wait_warp(empty, (n - 1) & 1, p.err)) {
                     s_abort = 1;
                     ok = false;
                     continue;
@@ -255,11 +255,11 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         }
         // no copy may outlive the CTA: wait (bounded) for the last one per stage
         for (int st = 0; st < 2; ++st) {
-            if (last_k[st]) mbar_wait(&k_full[st], (last_k[st] - 1) & 1, p.err);
-            if (last_v[st]) mbar_wait(&v_full[st], (last_v[st] - 1) & 1, p.err);
+            if (last_k[st]) mbar_wait_warp(&k_full[st], (last_k[st] - 1) & 1, p.err);
+            if (last_v[st]) mbar_wait_warp(&v_full[st], (last_v[st] - 1) & 1, p.err);
         }
         if (which == 0)
-            for (uint32_t k = q_it > 2 ? q_it - 2 : 0; k < q_it; ++k) mbar_wait(&q_full[k & 1], (k >> 1) & 1, p.err);
+            for (uint32_t k = q_it > 2 ? q_it - 2 : 0; k < q_it; ++k) mbar_wait_warp(&q_full[k & 1], (k >> 1) & 1, p.err);
     } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------------------ MMA issuers
         // warp 1 issues S_k = Q K^T for tile t (k = t % 2) once the K tile is
@@ -348,14 +348,14 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         const float sl2 = p.scale_log2;
         uint32_t n_s = 0;  // S tiles of this warpgroup (all units)
         uint32_t kv_it = 0, q_it = 0;
-        for (int u = blockIdx.x; u < num_units && !s_abort; u += gridDim.x, ++q_it) {
+        for (int u = blockIdx.x; u < num_units && !warp_flag(s_abort); u += gridDim.x, ++q_it) {
             const FaUnit U = fa_unit(p, u);  // the softmax waits for S anyway: no prefetch
             const int qi = U.row0 + row;  // query index within the request's new tokens
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
             const uint32_t kv_base = kv_it;
             for (int t = k; t < U.ntiles; t += 2) {
-                if (!mbar_wait(&s_full[k], n_s & 1, p.err)) { ok = false; break; }
+                if (!mbar_wait_warp(&s_full[k], n_s & 1, p.err)) { ok = false; break; }
                 tc_fence_after();
                 const int kb = U.kb0 + t * BN;
                 const bool edge = (U.slot == 0) ? (kb + BN - 1 > U.row0 || kb + BN > U.c1)
@@ -424,8 +424,11 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 if (edge) tile_body(std::true_type{});
                 else tile_body(std::false_type{});
                 l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                // O_k's previous product finished before this S tile was computed
-                if (rescale) {
+                // O_k's previous product finished before this S tile was computed.
+                // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
+                // takes this branch if any of its rows needs the rescale (alpha
+                // stays 1 for the others)
+                if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
                     for (int c = 0; c < D / 16; ++c) {
                         uint32_t r[16];
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 // hold anything (other positions, NaN-poisoned slots): zero them
                 if (U.slot != 0 && kb + BN > U.c1) {
                     const uint32_t vi = kv_base + t;
-                    if (!mbar_wait(&v_full[vi & 1], (vi >> 1) & 1, p.err)) { ok = false; break; }
+                    if (!mbar_wait_warp(&v_full[vi & 1], (vi >> 1) & 1, p.err)) { ok = false; break; }
                     const int valid = U.c1 - kb;
                     uint8_t* vt = smem + C::kOffV + (vi & 1) * C::kKVBytes;
                     for (int ci = wg_tid; ci < (BN - valid) * (D / 8); ci += 128) {
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             // ---- epilogue: merge the two warpgroups' (max, sum, O) like two KV splits
             const FaUnit E = fa_unit(p, u);  // re-read rather than kept live through the tile loop
             const int n_mine = (E.ntiles - k + 1) / 2, n_other = (E.ntiles - (1 - k) + 1) / 2;
-            if (n_mine > 0 && !mbar_wait(&pv_done[k], (n_s - 1) & 1, p.err)) {
+            if (n_mine > 0 && !mbar_wait_warp(&pv_done[k], (n_s - 1) & 1, p.err)) {
                 s_abort = 1;
                 break;
             }
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ml_ready);
-            if (!mbar_wait(ml_ready, q_it & 1, p.err)) {
+            if (!mbar_wait_warp(ml_ready, q_it & 1, p.err)) {
                 s_abort = 1;
                 break;
             }

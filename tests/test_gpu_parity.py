@@ -69,6 +69,45 @@ def test_decode_mla(Hq, bs):
     check_batch(W.make_batch(spec))
 
 
+def test_decode_mla_two_head_groups():
+    """256 heads: two groups of 128 heads per split on the tensor-core kernel."""
+    spec = _dec("mla_256", [0, 63, 64, 65, 1100], 256, 1, 576, 16, seed=256, mla=True, dv=512)
+    check_batch(W.make_batch(spec))
+
+
+def _amplify_keys(batch, r, lo, hi, factor, dims=slice(None)):
+    """Scale dims `dims` of keys [lo, hi) of request r (bf16 round trip) so that,
+    for some rows and not others, the running max jumps by more than 2^8
+    mid-sequence: the lazy O rescale then runs for part of a warp's rows only."""
+    rows = batch.seq_start[r] + np.arange(lo, hi)
+    f = W.bf16_bits_to_f32(batch.k_seq[rows])
+    f[..., dims] *= np.float32(factor)
+    batch.k_seq[rows] = W.to_bf16_bits(f)
+
+
+def test_decode_mla_rescale_some_heads():
+    # split 1 of request 0 (keys 1024..2047) meets a band at 1500 whose last 64
+    # latent dims (scores only; the value is dims 0..511, left as drawn, so
+    # |O| stays O(1)) are amplified: 43 of 128 heads, in all four warps, must
+    # rescale O
+    spec = W.spec_custom("mla_rs", ctx=[2999, 1999], qlen=[1, 1], num_decodes=2, num_extends=0,
+                         num_prefills=0, Hq=128, Hkv=1, d=576, dv=512, bs=64, scale=1 / np.sqrt(192),
+                         mla=True, seed=5)
+    batch = W.make_batch(spec)
+    _amplify_keys(batch, 0, 1500, 1564, 7.0, dims=slice(512, 576))
+    check_batch(batch)
+
+
+def test_prefill_rescale_some_rows():
+    # keys 600..639 amplified: about a third of the rows that see them, in
+    # every warp, must rescale O mid-sequence
+    spec = W.spec_custom("fa_rs", ctx=[0], qlen=[1000], num_decodes=0, num_extends=0, num_prefills=1,
+                         Hq=16, Hkv=2, d=128, dv=128, bs=16, seed=6)
+    batch = W.make_batch(spec)
+    _amplify_keys(batch, 0, 600, 640, 3.5)
+    check_batch(batch)
+
+
 def test_decode_mla_many_units():
     """More (request, split, half) units than SMs, several splits per request."""
     rng = np.random.default_rng(17)
