@@ -142,6 +142,12 @@ PKA_DEVICE void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
                  : "memory");
 }
 
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address.
+PKA_DEVICE void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 PKA_DEVICE void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),

@@ -32,6 +32,8 @@
 // S row -> online softmax (the O rescale is lazy: only when the max grew by
 // more than 2^8) -> P into TMEM; at the end of a unit O / l goes to out, or
 // to the fp32 split partials + LSE that the decode reduction merges.
+#include <type_traits>
+
 #include "common.cuh"
 #include "params.cuh"
 #include "plan.cuh"
@@ -41,6 +43,7 @@ namespace pka {
 
 constexpr int kMtThreads = 192;
 constexpr int kMtTile = 64;                       // keys per tile (the N of S)
+constexpr int kMtPrefetch = 2;                    // tiles of L2 prefetch ahead of the copies
 constexpr int kMtD = 576, kMtDv = 512, kMtHalf = 256;
 constexpr int kMtQtDims = 320;                    // q dims held in TMEM
 constexpr int kMtChunk = kMtTile * 128;           // one 64-dim column chunk of a tile (8 KB)
@@ -83,8 +86,13 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMtOffBar);
-    uint64_t* kv_full = bars + 0;    // [2] per latent stage
-    uint64_t* kv_empty = bars + 2;   // [2]
+    // A latent stage is two parts with their own barriers: the value chunks
+    // this unit's P . V reads, and the other (score-only) chunks, which are
+    // free again as soon as the first part of S has read them.
+    uint64_t* kv_full = bars + 0;     // [2] score-only chunks landed
+    uint64_t* kv_empty = bars + 2;    // [2] score-only chunks read by S
+    uint64_t* kv_full_v = bars + 16;  // [2] value chunks landed
+    uint64_t* kv_empty_v = bars + 18; // [2] value chunks read by S and P . V
     uint64_t* u_full = bars + 4;     // [2] unit ring slot written
     uint64_t* u_empty = bars + 6;    // [2] unit ring slot read by the issuer and the 4 softmax warps
     uint64_t* q_full = bars + 8;     // q[:, 320:576] landed in shared memory
@@ -108,6 +116,8 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
+            mbar_init(&kv_full_v[i], 1);
+            mbar_init(&kv_empty_v[i], 1);
             mbar_init(&u_full[i], 1);
             mbar_init(&u_empty[i], 5);
         }
@@ -180,54 +190,108 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             }
             ++q_it;
             const int32_t* bt = p.block_table + (int64_t)U.r * p.max_blocks;
+            // validated block id of key position `pos` of this request
+            auto block_of = [&](int pos) -> int {
+                int blk = __ldg(bt + pos / p.bs);
+                if (blk < 0 || blk >= p.num_blocks) {
+                    set_error(p.err, PKA_DEVERR_BLOCK_ID);
+                    blk = 0;
+                }
+                return blk;
+            };
             bool ok = true;
+            const uint32_t vmask = U.half ? 0xF0u : 0x0Fu;  // chunks holding this half's value dims
             for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
                 const int st = kv_it & 1;
                 const uint32_t n = kv_it >> 1;
-                if (n > 0 && !mbar_wait_warp(&kv_empty[st], (n - 1) & 1, p.err)) {
-                    ok = false;
-                    break;
+                // L2 prefetch of the tile kMtPrefetch ahead (its stage is still
+                // busy), so the copy that refills a freed stage reads from L2
+                if (t + kMtPrefetch < U.ntiles) {
+                    const int pb = U.k0 + (t + kMtPrefetch) * kMtTile;
+                    const int pv = min(kMtTile, U.k1 - pb);
+                    if (use_tma) {
+                        const int rows = p.bs < kMtTile ? p.bs : kMtTile;
+                        const int nbox = (pv + rows - 1) / rows;
+                        if (lane < nbox) {
+                            const int pos = pb + lane * rows;
+                            const int row = block_of(pos) * p.bs + (pos % p.bs);
+                            for (int c = 0; c < 9; ++c) tma_prefetch_2d(&kvmap, c * 64, row);
+                        }
+                    } else {
+                        for (int r = lane; r < pv; r += 32) {
+                            const int pos = pb + r;
+                            bulk_prefetch_l2(p.kv + ((int64_t)block_of(pos) * p.bs + pos % p.bs) * kMtD, kMtD * 2);
+                        }
+                    }
                 }
                 uint8_t* dst = smem + kMtOffKV + st * kMtTileBytes;
                 const int tb = U.k0 + t * kMtTile;
                 const int valid = min(kMtTile, U.k1 - tb);
-                if (use_tma && valid == kMtTile) {
-                    const int rows = p.bs < kMtTile ? p.bs : kMtTile;  // rows per box
-                    const int nbox = kMtTile / rows;
-                    if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], kMtTileBytes);
-                    __syncwarp();
-                    if (lane < nbox) {  // one lane per box, in parallel
-                        const int pos = tb + lane * rows;
-                        int blk = __ldg(bt + pos / p.bs);
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            set_error(p.err, PKA_DEVERR_BLOCK_ID);
-                            blk = 0;
-                        }
-                        const int row = blk * p.bs + (pos % p.bs);
-                        for (int c = 0; c < 9; ++c)
-                            tma_load_2d(dst + c * kMtChunk + lane * rows * 128, &kvmap, &kv_full[st], c * 64, row, pol);
+                const bool tma = use_tma && valid == kMtTile;
+                const int blk_lo = (!tma && tb + lane < U.k1) ? block_of(tb + lane) : 0;
+                const int blk_hi = (!tma && tb + 32 + lane < U.k1) ? block_of(tb + 32 + lane) : 0;
+                // part 0: the score-only chunks, part 1: the value chunks
+                for (int part = 0; part < 2; ++part) {
+                    uint64_t* empty = part ? &kv_empty_v[st] : &kv_empty[st];
+                    uint64_t* full = part ? &kv_full_v[st] : &kv_full[st];
+                    const uint32_t cmask = part ? vmask : (0x1FFu & ~vmask);
+                    if (n > 0 && !mbar_wait_warp(empty, (n - 1) & 1, p.err)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-                    // 16-byte copies; rows past the split's end are zero-filled
-                    // (no NaN from slots the batch does not own)
-                    const uint32_t dbase = smem_u32(dst);
-                    for (int ci = lane; ci < kMtTile * (kMtD / 8); ci += 32) {
-                        const int tr = ci / (kMtD / 8), c = ci % (kMtD / 8);
-                        const int pos = tb + tr;
-                        const bool in = pos < U.k1;
-                        int blk = in ? __ldg(bt + pos / p.bs) : 0;
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            set_error(p.err, PKA_DEVERR_BLOCK_ID);
-                            blk = 0;
+                    if (tma) {
+                        const int rows = p.bs < kMtTile ? p.bs : kMtTile;  // rows per box
+                        const int nbox = kMtTile / rows;
+                        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(__popc(cmask) * kMtChunk));
+                        __syncwarp();
+                        if (lane < nbox) {  // one lane per box, in parallel
+                            const int pos = tb + lane * rows;
+                            const int row = block_of(pos) * p.bs + (pos % p.bs);
+                            for (int c = 0; c < 9; ++c)
+                                if ((cmask >> c) & 1)
+                                    tma_load_2d(dst + c * kMtChunk + lane * rows * 128, &kvmap, full, c * 64, row, pol);
                         }
-                        const int64_t row = (int64_t)blk * p.bs + (in ? pos % p.bs : 0);
-                        cp_async_16_zfill(dbase + (c >> 3) * kMtChunk + sw128(tr, c & 7), p.kv + row * kMtD + c * 8, in);
+                    } else {
+                        // 16-byte copies, the whole warp on one row at a time (512
+                        // contiguous bytes per instruction); the rows' block ids were
+                        // loaded once, two per lane, and are shuffled to the warp.
+                        // Rows past the split's end are zero-filled (no NaN from
+                        // slots the batch does not own).
+                        const uint32_t dbase = smem_u32(dst);
+                        const int npieces = 8 * __popc(cmask);
+                        // this lane's pieces: chunk and 16-byte index within the chunk
+                        int pc[2], pk[2];
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int pi = lane + 32 * j;
+                            int nth = pi >> 3, c = 0;
+                            for (int cc = 0; cc < 9; ++cc)
+                                if ((cmask >> cc) & 1) {
+                                    if (nth == 0) c = cc;
+                                    --nth;
+                                }
+                            pc[j] = c;
+                            pk[j] = pi & 7;
+                        }
+                        for (int tr = 0; tr < kMtTile; ++tr) {
+                            const int b_lo = __shfl_sync(0xffffffffu, blk_lo, tr & 31);
+                            const int b_hi = __shfl_sync(0xffffffffu, blk_hi, tr & 31);
+                            const int pos = tb + tr;
+                            const bool in = pos < U.k1;
+                            const __nv_bfloat16* src =
+                                p.kv + ((int64_t)(tr < 32 ? b_lo : b_hi) * p.bs + (in ? pos % p.bs : 0)) * kMtD;
+#pragma unroll
+                            for (int j = 0; j < 2; ++j)
+                                if (lane + 32 * j < npieces)
+                                    cp_async_16_zfill(dbase + pc[j] * kMtChunk + sw128(tr, pk[j]),
+                                                      src + pc[j] * 64 + pk[j] * 8, in);
+                        }
+                        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(full)) : "memory");
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(full);
                     }
-                    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&kv_full[st]))
-                                 : "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&kv_full[st]);
                 }
+                if (!ok) break;
                 last[st] = n + 1;
             }
             if (!ok) {
@@ -237,7 +301,10 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         }
         // no copy may outlive the CTA: wait (bounded) for the last one per stage
         for (int st = 0; st < 2; ++st)
-            if (last[st]) mbar_wait_warp(&kv_full[st], (last[st] - 1) & 1, p.err);
+            if (last[st]) {
+                mbar_wait_warp(&kv_full[st], (last[st] - 1) & 1, p.err);
+                mbar_wait_warp(&kv_full_v[st], (last[st] - 1) & 1, p.err);
+            }
         if (q_it > 0) mbar_wait_warp(q_full, (q_it - 1) & 1, p.err);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -246,22 +313,32 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         const uint32_t q_s = sm_base + kMtOffQ, kv_s = sm_base + kMtOffKV;
         uint32_t kv_it = 0, s_it = 0, pv_it = 0, q_it = 0;
         bool ok = true;
-        // S = q . C^T over all 576 dims: 20 k-steps with A (q[:, 0:320]) in
-        // TMEM, 16 with A (q[:, 320:576]) in shared memory
-        auto issue_s = [&](uint32_t kvi) {
+        // S = q . C^T over all 576 dims, in two parts: the score-only chunks
+        // first (their stage part is released right after), then the value
+        // chunks. k-steps over q[:, 0:320] take A from TMEM, the rest from
+        // shared memory. The chunk sets are fixed per value half, so each part
+        // is straight-line code.
+        auto issue_s_part = [&](uint32_t kvi, auto half_c, auto part_c) {
+            constexpr int H = decltype(half_c)::value, PART = decltype(part_c)::value;
+            constexpr int first_c = H ? 0 : 4;  // first chunk of part 0: it starts the accumulation
             const uint32_t kv = kv_s + (kvi & 1) * kMtTileBytes;
 #pragma unroll
-            for (int ks = 0; ks < kMtQtDims / 16; ++ks)
-                umma_bf16_ts(tbase + kMtColS, tbase + kMtColQ + ks * 8,
-                             umma_desc_sw128(kv + (ks >> 2) * kMtChunk + (ks & 3) * 32, 16, 1024), idesc_s,
-                             ks > 0 ? 1u : 0u);
+            for (int c = 0; c < 9; ++c) {
+                const bool vchunk = H ? (c >= 4 && c < 8) : (c < 4);
+                if (vchunk != (PART == 1)) continue;
 #pragma unroll
-            for (int ks = kMtQtDims / 16; ks < kMtD / 16; ++ks) {
-                const int kq = ks - kMtQtDims / 16;
-                umma_bf16(tbase + kMtColS, umma_desc_sw128(q_s + (kq >> 2) * kMtQsChunk + (kq & 3) * 32, 16, 1024),
-                          umma_desc_sw128(kv + (ks >> 2) * kMtChunk + (ks & 3) * 32, 16, 1024), idesc_s, 1u);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int ks = 4 * c + kk;
+                    const uint64_t bdesc = umma_desc_sw128(kv + c * kMtChunk + kk * 32, 16, 1024);
+                    const uint32_t acc = (PART == 0 && c == first_c && kk == 0) ? 0u : 1u;
+                    if (c < kMtQtDims / 64)
+                        umma_bf16_ts(tbase + kMtColS, tbase + kMtColQ + ks * 8, bdesc, idesc_s, acc);
+                    else
+                        umma_bf16(tbase + kMtColS,
+                                  umma_desc_sw128(q_s + (c - kMtQtDims / 64) * kMtQsChunk + kk * 32, 16, 1024), bdesc,
+                                  idesc_s, acc);
+                }
             }
-            umma_commit(s_full);
         };
         // O(half) += P . C[:, half*256 .. +256)
         auto issue_o = [&](uint32_t kvi, int half, bool first) -> bool {
@@ -275,7 +352,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 umma_bf16_ts(tbase + kMtColO, tbase + kMtColP + kk * 8, umma_desc_sw128(v + kk * 16 * 128, kMtChunk, 1024),
                              idesc_o, (!first || kk > 0) ? 1u : 0u);
             umma_commit(pv_done);
-            umma_commit(&kv_empty[kvi & 1]);
+            umma_commit(&kv_empty_v[kvi & 1]);
             ++pv_it;
             return true;
         };
@@ -295,13 +372,23 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 } else {
                     const uint32_t kv_base = kv_it;
                     for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
-                        if (!mbar_wait(&kv_full[kv_it & 1], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                        const int st = kv_it & 1;
+                        if (!mbar_wait(&kv_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
                         if (s_it > 0 && !mbar_wait(s_free, (s_it - 1) & 1, p.err)) { ok = false; break; }
                         tc_fence_after();
-                        issue_s(kv_it);
+                        if (U.half) issue_s_part(kv_it, std::integral_constant<int, 1>{}, std::integral_constant<int, 0>{});
+                        else issue_s_part(kv_it, std::integral_constant<int, 0>{}, std::integral_constant<int, 0>{});
+                        umma_commit(&kv_empty[st]);  // score-only chunks free once read
+                        // O += P . V of the previous tile goes between the two parts of
+                        // S: its value chunks are then released a whole S part earlier
+                        if (t > 0 && !issue_o(kv_it - 1, U.half, t == 1)) { ok = false; break; }
+                        if (!mbar_wait(&kv_full_v[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                        tc_fence_after();
+                        if (U.half) issue_s_part(kv_it, std::integral_constant<int, 1>{}, std::integral_constant<int, 1>{});
+                        else issue_s_part(kv_it, std::integral_constant<int, 0>{}, std::integral_constant<int, 1>{});
+                        umma_commit(s_full);
                         ++s_it;
                         if (t == U.ntiles - 1) umma_commit(q_empty);
-                        if (t > 0 && !issue_o(kv_it - 1, U.half, t == 1)) { ok = false; break; }
                     }
                     if (ok && !issue_o(kv_base + U.ntiles - 1, U.half, U.ntiles == 1)) ok = false;
                 }
