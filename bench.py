@@ -232,11 +232,15 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
     """Prefill, mixed and MLA workloads, timed one after the other."""
     import torch
     res = {}
-    cases = [("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20),
-             ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0),
-             ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0),
-             ("mla_decode_bs1", W.spec_mla_decode(block_size=1), "decode", "hbm", 0)]
-    for name, spec, dom, bound, flush in cases:
+    # (name, spec, dominant kernel, bound, L2 flush bytes, committed ncu traffic entry)
+    cases = [("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20,
+              ("fa_fwd.cu", "fa_fwd_prefill_varlen")),
+             ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0, None),
+             ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0,
+              ("decode_mla_tc.cu", "decode_mla_tc_mla_decode_bs64")),
+             ("mla_decode_bs1", W.spec_mla_decode(block_size=1), "decode", "hbm", 0, None)]
+    for name, spec, dom, bound, flush, tkey in cases:
+        traffic = kernel_traffic(*tkey) if tkey else None
         db = make_device_batch(spec, device, seed=1234 + rank)
         ms, stats, launches, _ = time_steps(db, steps, warmup, flush_bytes=flush)
         w = algorithmic_work(spec)
@@ -248,7 +252,7 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
             ent["tflops_step"] = round(flops / (ms * 1e-3) / 1e12, 2)
             if kms:
                 ent["roofline"] = roofline("tensor", flops / (kms * 1e-3) / 1e12, peaks["bf16_tflops"],
-                                           "TFLOP/s", None)
+                                           "TFLOP/s", traffic)
             if w["dec_bytes"]:
                 dk = stats.get("decode", {}).get("avg_ms")
                 if dk:
@@ -257,7 +261,7 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
             ent["kv_gbs_step"] = round(w["dec_bytes"] / (ms * 1e-3) / 1e9, 1)
             if kms:
                 ent["roofline"] = roofline("hbm", w["dec_bytes"] / (kms * 1e-3) / 1e9, peaks["hbm_gbs"],
-                                           "GB/s", None)
+                                           "GB/s", traffic)
                 ent["tflops_decode_kernel"] = round(w["dec_flops"] / (kms * 1e-3) / 1e12, 1)
         res[name] = ent
         del db
