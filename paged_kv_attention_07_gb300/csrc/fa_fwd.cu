@@ -8,34 +8,35 @@
 //            precedes the new tokens), each emitting (O, LSE) for the merge.
 // The pages gather each context chunk into a contiguous buffer first
 // (cp_mha_gather_cache); here TMA boxes walk the block table directly, and
-// the chunk loop is a grid dimension: every (query tile, chunk) is an
+// the chunk loop is a grid dimension: every (query tiles, chunk) is an
 // independent work item, merged afterwards by the extend reduction.
 //
-// Work unit: (request, 128-row query tile, slot) x query head, slot 0 = new
-// keys, slot c >= 1 = context chunk c - 1. Persistent CTAs (one per SM) walk
-// the planner's cost-sorted unit list round-robin. Per CTA, 12 warps:
-//   warp 0   TMA producer of the Q tile (double-buffered) and the K tiles of
-//            128 keys (2-stage ring); warp 2 the same for the V tiles (block
-//            sizes below 8 use cp.async copies);
-//   warp 1   tensor-memory owner; one thread issues S = Q K^T;
-//   warp 3   one thread issues O += P V (A operand P read from TMEM);
-//   warps 4-7, 8-11: two softmax warpgroups, one thread per query row (=
-//            TMEM lane). Warpgroup k takes the unit's key tiles t = k, k+2,
-//            ... with its own S buffer S_k, its own running max and sum and
-//            its own accumulator O_k, so one warpgroup's exponentials overlap
-//            the other's waits, loads and stores. Each reads its S row twice
-//            (row max, then exponentials: the row never has to sit in
-//            registers whole), writes P as bf16 pairs over the S_k columns it
-//            has already consumed, and rescales O_k only when its max grew by
-//            more than 2^8 (otherwise the stale max is kept: P stays <= 2^8).
-//            At the end of a unit the two (max, sum, O) are merged exactly
-//            like two KV splits (the LSE merge), each warpgroup producing half
-//            of the head_dim columns of out (+ LSE).
-// TMEM holds S0, S1 (128 fp32 columns each) and O0, O1 (head_dim fp32 columns
-// each): 512 columns. The S = Q K^T that refills S_k waits for the P . V that
-// read P_k, so a warpgroup that sees its S tile may also touch O_k freely.
-// Every barrier belongs to one buffer or one warpgroup and cannot complete
-// twice before its waiter looks, so mbarrier phase parities never alias.
+// Work unit: (request, two adjacent 128-row query tiles, slot) x query head,
+// slot 0 = new keys, slot c >= 1 = context chunk c - 1. Persistent CTAs (one
+// per SM) walk the planner's cost-sorted unit list round-robin. Per CTA, 12
+// warps:
+//   warp 0   TMA producer of the K tiles of 128 keys (2-stage ring);
+//   warp 2   the same for the V tiles, and the unit's two Q tiles (block
+//            sizes below 8 use cp.async copies for K and V);
+//   warp 1   tensor-memory owner; one thread issues S_k = Q_k K^T for both
+//            query tiles k of every K tile;
+//   warp 3   one thread issues O_k += P_k V (A operand P_k read from TMEM);
+//   warps 4-7, 8-11: softmax warpgroup k owns query tile k, one thread per
+//            query row (= TMEM lane), with its own S_k, running max and sum
+//            and O_k. Each reads its S row twice (row max, then exponentials:
+//            the row never sits in registers whole), writes P as bf16 pairs
+//            over the S_k columns it has already consumed, rescales O_k only
+//            when its max grew by more than 2^8 (otherwise the stale max is
+//            kept: P stays <= 2^8; warp-uniform, tcgen05.ld/st being
+//            warp-collective), and ends the unit on its own: O_k / l to out
+//            (+ LSE) or to the extend partials.
+// Both query tiles consume every K and V tile once from shared memory, and
+// the two warpgroups' exponentials overlap each other's waits. TMEM holds S0,
+// S1 (128 fp32 columns each) and O0, O1 (head_dim fp32 columns each): 512
+// columns. The S_k = Q_k K^T that refills S_k waits for the P_k . V that read
+// P_k, so a warpgroup that sees its S tile may also touch O_k freely. Every
+// barrier belongs to one buffer or one warpgroup and cannot complete twice
+// before its waiter looks, so mbarrier phase parities never alias.
 #include <type_traits>
 
 #include "common.cuh"
@@ -46,17 +47,17 @@
 namespace pka {
 
 constexpr int kFaThreads = 384;
-constexpr int BM = kFaBlockM;  // 128 query rows per unit
+constexpr int BM = kFaBlockM;  // 128 query rows per query tile
 constexpr int BN = kFaBlockN;  // 128 keys per tile
-static_assert(BM == 128 && BN == 128, "tile shape is fixed by the TMEM lane count");
+static_assert(BM == 128 && BN == 128 && kFaItemTiles == 2, "tile shape is fixed by the TMEM lane count");
 
 template <int D>
 struct FaCfg {
     static constexpr int kChunks = D / 64;                // 64-wide swizzle chunks per row
     static constexpr int kChunkBytes = 128 * 128;         // 128 rows x 128 B
-    static constexpr int kQBytes = kChunks * kChunkBytes;
+    static constexpr int kQBytes = kChunks * kChunkBytes;  // one query tile
     static constexpr int kKVBytes = kChunks * kChunkBytes;  // one K or V tile
-    static constexpr int kOffQ = 0;                        // two Q buffers
+    static constexpr int kOffQ = 0;                        // the unit's two query tiles
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
     static constexpr int kOffV = kOffK + 2 * kKVBytes;
     static constexpr int kOffBar = kOffV + 2 * kKVBytes;
@@ -67,8 +68,9 @@ struct FaCfg {
 };
 
 struct FaUnit {
-    int r, slot, h, g, q0, qlen, ctx, row0;
-    int kb0, ntiles, c0, c1;  // first tile's key base, tiles, visible keys [c0, c1)
+    int r, slot, h, g, q0, qlen, ctx, row0;  // row0: first row of query tile 0
+    int kb0, c0, c1, nkv;                     // first tile's key base, visible keys [c0, c1), key tiles
+    int c1k[2], ntk[2];                       // per query tile: end of its visible keys, its key tiles (0: no rows)
 };
 
 PKA_DEVICE FaUnit fa_unit(const FaParams& p, int u) {
@@ -81,17 +83,23 @@ PKA_DEVICE FaUnit fa_unit(const FaParams& p, int u) {
     U.q0 = p.qsl[U.r];
     U.qlen = p.qsl[U.r + 1] - U.q0;
     U.ctx = p.seq_lens[U.r] - U.qlen;
-    U.row0 = it.y * BM;
+    U.row0 = it.y * kFaItemRows;
     if (U.slot == 0) {
         U.c0 = 0;
-        U.c1 = min(U.qlen, U.row0 + BM);
         U.kb0 = 0;
+        for (int k = 0; k < 2; ++k) {
+            const int rk = U.row0 + k * BM;
+            U.c1k[k] = rk < U.qlen ? min(U.qlen, rk + BM) : 0;
+        }
+        U.c1 = max(U.c1k[0], U.c1k[1]);
     } else {
         U.c0 = (U.slot - 1) * p.chunk;
         U.c1 = min(U.ctx, U.c0 + p.chunk);
         U.kb0 = (U.c0 / BN) * BN;
+        for (int k = 0; k < 2; ++k) U.c1k[k] = U.row0 + k * BM < U.qlen ? U.c1 : 0;
     }
-    U.ntiles = (U.c1 - U.kb0 + BN - 1) / BN;
+    for (int k = 0; k < 2; ++k) U.ntk[k] = U.c1k[k] > 0 ? (U.c1k[k] - U.kb0 + BN - 1) / BN : 0;
+    U.nkv = max(U.ntk[0], U.ntk[1]);
     return U;
 }
 
@@ -115,29 +123,27 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-    uint64_t* q_full = bars + 0;     // [2] per Q buffer
-    uint64_t* q_empty = bars + 2;    // [2]
-    uint64_t* k_full = bars + 4;     // [2] per K stage
-    uint64_t* k_empty = bars + 6;    // [2]
-    uint64_t* v_full = bars + 8;     // [2] per V stage
-    uint64_t* v_empty = bars + 10;   // [2]
-    uint64_t* s_full = bars + 12;    // [2] per softmax warpgroup: its S tile is in TMEM
-    uint64_t* p_full = bars + 14;    // [2] its P is in TMEM (4 warp arrivals)
-    uint64_t* pv_done = bars + 16;   // [2] the P . V that read its P is done
-    uint64_t* o_free = bars + 18;    // the unit's epilogue has read O0 and O1 (8 warp arrivals)
-    uint64_t* ml_ready = bars + 19;  // both warpgroups' row max and sum are published (8 warp arrivals)
+    uint64_t* q_full = bars + 0;     // the unit's query tiles landed
+    uint64_t* q_empty = bars + 1;    // the unit's last S product is done
+    uint64_t* k_full = bars + 2;     // [2] per K stage
+    uint64_t* k_empty = bars + 4;    // [2]
+    uint64_t* v_full = bars + 6;     // [2] per V stage
+    uint64_t* v_empty = bars + 8;    // [2]
+    uint64_t* s_full = bars + 10;    // [2] per softmax warpgroup: its S tile is in TMEM
+    uint64_t* p_full = bars + 12;    // [2] its P is in TMEM (4 warp arrivals)
+    uint64_t* pv_done = bars + 14;   // [2] the P . V that read its P is done
+    uint64_t* o_free = bars + 16;    // [2] its epilogue has read O_k (4 warp arrivals)
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
-    __shared__ float2 s_ml[2][2][BM];  // [unit parity][warpgroup][row] = (max, sum)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_units = p.hdr->fa_num_items * p.Hq;
     if (num_units == 0) return;
 
     if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 1);
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
@@ -145,9 +151,8 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
+            mbar_init(&o_free[i], 4);
         }
-        mbar_init(o_free, 8);
-        mbar_init(ml_ready, 8);
         fence_barrier_init();
         s_abort = 0;
         tma_prefetch_desc(&maps.q);
@@ -165,41 +170,45 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers
-        // warp 0 loads Q and K tiles, warp 2 loads V tiles (so a V load that
-        // waits for an older P . V never delays the next K). K/V lines stay
-        // in L2 with normal priority: every context chunk is read by all the
-        // query heads of its KV head and all query tiles of its request.
-        const int which = warp == 0 ? 0 : 1;  // 0 = K (+ Q), 1 = V
+        // warp 0 loads K tiles, warp 2 the query tiles and V tiles (so a V load
+        // that waits for an older P . V never delays the next K). K/V lines
+        // stay in L2 with normal priority: every context chunk is read by all
+        // the query heads of its KV head and all query tiles of its request.
+        const int which = warp == 0 ? 0 : 1;  // 0 = K, 1 = V (+ Q)
         const uint64_t pol_kv = policy_evict_normal();
         const uint64_t pol_q = policy_evict_last();
         const bool ctx_tma = p.bs >= 8;
         uint32_t kv_it = 0, q_it = 0;
-        uint32_t last_k[2] = {0, 0}, last_v[2] = {0, 0};  // phase + 1 of the last copy per stage (0 = none)
+        uint32_t last[2] = {0, 0};  // phase + 1 of the last copy per stage (0 = none)
         FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
         for (int u = blockIdx.x; u < num_units && !warp_flag(s_abort); u += gridDim.x, ++q_it) {
             const FaUnit U = Un;
             if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);  // prefetch
-            const int qb = q_it & 1;
-            if (which == 0 && q_it >= 2 && !mbar_wait_warp(&q_empty[qb], ((q_it >> 1) - 1) & 1, p.err)) {
-                s_abort = 1;
-                break;
-            }
-            if (which == 0 && lane == 0) {
-                mbar_arrive_expect_tx(&q_full[qb], C::kQBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffQ + qb * C::kQBytes + c * C::kChunkBytes, &maps.q, &q_full[qb], c * 64,
-                                U.h, U.q0 + U.row0, pol_q);
+            if (which == 1) {
+                // the previous unit's S products are done with the query tiles
+                if (q_it > 0 && !mbar_wait_warp(q_empty, (q_it - 1) & 1, p.err)) {
+                    s_abort = 1;
+                    break;
+                }
+                if (lane == 0) {
+                    const int nq = U.ntk[1] > 0 ? 2 : 1;
+                    mbar_arrive_expect_tx(q_full, (uint32_t)(nq * C::kQBytes));
+                    for (int k = 0; k < nq; ++k)
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(smem + C::kOffQ + k * C::kQBytes + c * C::kChunkBytes, &maps.q, q_full,
+                                        c * 64, U.h, U.q0 + U.row0 + k * BM, pol_q);
+                }
             }
             const int32_t* bt = p.block_table + (int64_t)U.r * p.max_blocks;
             const bool paged_tma = U.slot != 0 && ctx_tma;
             int blk_next = paged_tma ? tile_block_id(p, bt, U.kb0, U.c1, lane) : 0;
             bool ok = true;
-            for (int t = 0; t < U.ntiles && ok; ++t, ++kv_it) {
+            for (int t = 0; t < U.nkv && ok; ++t, ++kv_it) {
                 const int st = kv_it & 1;
                 const uint32_t n = kv_it >> 1;
                 const int kb = U.kb0 + t * BN;
                 const int blk_mine = blk_next;  // block ids of this tile, one per lane
-                if (paged_tma && t + 1 < U.ntiles) blk_next = tile_block_id(p, bt, kb + BN, U.c1, lane);
+                if (paged_tma && t + 1 < U.nkv) blk_next = tile_block_id(p, bt, kb + BN, U.c1, lane);
                 uint64_t* full = which ? &v_full[st] : &k_full[st];
                 uint64_t* empty = which ? &v_empty[st] : &k_empty[st];
                 if (n > 0 && !mbar_wait_warp(empty, (n - 1) & 1, p.err)) {
@@ -248,23 +257,19 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     __syncwarp();
                     if (lane == 0) mbar_arrive(full);
                 }
-                if (which) last_v[st] = n + 1;
-                else last_k[st] = n + 1;
+                last[st] = n + 1;
             }
             if (!ok) break;
         }
         // no copy may outlive the CTA: wait (bounded) for the last one per stage
-        for (int st = 0; st < 2; ++st) {
-            if (last_k[st]) mbar_wait_warp(&k_full[st], (last_k[st] - 1) & 1, p.err);
-            if (last_v[st]) mbar_wait_warp(&v_full[st], (last_v[st] - 1) & 1, p.err);
-        }
-        if (which == 0)
-            for (uint32_t k = q_it > 2 ? q_it - 2 : 0; k < q_it; ++k) mbar_wait_warp(&q_full[k & 1], (k >> 1) & 1, p.err);
+        for (int st = 0; st < 2; ++st)
+            if (last[st]) mbar_wait_warp(which ? &v_full[st] : &k_full[st], (last[st] - 1) & 1, p.err);
+        if (which == 1 && q_it > 0) mbar_wait_warp(q_full, (q_it - 1) & 1, p.err);
     } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------------------ MMA issuers
-        // warp 1 issues S_k = Q K^T for tile t (k = t % 2) once the K tile is
-        // in and the previous P_k . V (which read P_k out of S_k's columns)
-        // is done; warp 3 issues O_k += P_k V as each P_k lands. Each thread
+        // warp 1 issues S_k = Q_k K^T for both query tiles of every K tile, each
+        // once the previous P_k . V (which read P_k out of S_k's columns) is
+        // done; warp 3 issues O_k += P_k V as each P_k lands. Each thread
         // commits only its own MMAs.
         if (lane == 0 && warp == 1) {
             constexpr uint32_t idesc_qk = umma_idesc_bf16(128, 128, 0, 0);
@@ -276,28 +281,31 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x, ++q_it) {
                 const FaUnit U = Un;
                 if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
-                const int qb = q_it & 1;
-                if (!mbar_wait(&q_full[qb], (q_it >> 1) & 1, p.err)) {
+                if (!mbar_wait(q_full, q_it & 1, p.err)) {
                     ok = false;
                     break;
                 }
-                for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
+                for (int t = 0; t < U.nkv; ++t, ++kv_it) {
                     const int st = kv_it & 1;
-                    const int k = t & 1;
                     if (!mbar_wait(&k_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
-                    if (nq[k] > 0 && !mbar_wait(&pv_done[k], (nq[k] - 1) & 1, p.err)) { ok = false; break; }
-                    tc_fence_after();
+                    for (int k = 0; k < 2; ++k) {
+                        if (t >= U.ntk[k]) continue;
+                        if (nq[k] > 0 && !mbar_wait(&pv_done[k], (nq[k] - 1) & 1, p.err)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-                        umma_bf16(tbase + C::kColS + k * 128, umma_desc_sw128(q_s + qb * C::kQBytes + off, 16, 1024),
-                                  umma_desc_sw128(k_s + st * C::kKVBytes + off, 16, 1024), idesc_qk,
-                                  ks > 0 ? 1u : 0u);
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+                            umma_bf16(tbase + C::kColS + k * 128,
+                                      umma_desc_sw128(q_s + k * C::kQBytes + off, 16, 1024),
+                                      umma_desc_sw128(k_s + st * C::kKVBytes + off, 16, 1024), idesc_qk,
+                                      ks > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&s_full[k]);
+                        ++nq[k];
                     }
-                    umma_commit(&s_full[k]);
+                    if (!ok) break;
                     umma_commit(&k_empty[st]);
-                    if (t == U.ntiles - 1) umma_commit(&q_empty[qb]);
-                    ++nq[k];
+                    if (t == U.nkv - 1) umma_commit(q_empty);
                 }
             }
             if (!ok) s_abort = 1;
@@ -306,31 +314,38 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         } else if (lane == 0 && warp == 3) {
             constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, 0, 1);
             const uint32_t v_s = sm_base + C::kOffV;
-            uint32_t kv_it = 0, q_it = 0;
+            uint32_t kv_it = 0;
             uint32_t np[2] = {0, 0};  // products issued from P_k
+            uint32_t uo[2] = {0, 0};  // earlier units in which warpgroup k had rows (one epilogue each)
             bool ok = true;
             FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
-            for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x, ++q_it) {
+            for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x) {
                 const FaUnit U = Un;
                 if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
-                for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
+                for (int t = 0; t < U.nkv; ++t, ++kv_it) {
                     const int vs = kv_it & 1;
-                    const int k = t & 1;
-                    if (!mbar_wait(&p_full[k], np[k] & 1, p.err)) { ok = false; break; }
                     if (!mbar_wait(&v_full[vs], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
-                    // a unit's first products overwrite O0 / O1: the previous epilogue must have read them
-                    if (t == 0 && q_it > 0 && !mbar_wait(o_free, (q_it - 1) & 1, p.err)) { ok = false; break; }
-                    tc_fence_after();
+                    for (int k = 0; k < 2; ++k) {
+                        if (t >= U.ntk[k]) continue;
+                        if (!mbar_wait(&p_full[k], np[k] & 1, p.err)) { ok = false; break; }
+                        // a unit's first product overwrites O_k: its previous epilogue must have read it
+                        if (t == 0 && uo[k] > 0 && !mbar_wait(&o_free[k], (uo[k] - 1) & 1, p.err)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t bdesc = umma_desc_sw128(v_s + vs * C::kKVBytes + kk * 2048, C::kChunkBytes, 1024);
-                        umma_bf16_ts(tbase + C::kColO + k * D, tbase + C::kColS + k * 128 + kk * 8, bdesc, idesc_pv,
-                                     (t >= 2 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            const uint64_t bdesc =
+                                umma_desc_sw128(v_s + vs * C::kKVBytes + kk * 2048, C::kChunkBytes, 1024);
+                            umma_bf16_ts(tbase + C::kColO + k * D, tbase + C::kColS + k * 128 + kk * 8, bdesc,
+                                         idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(&pv_done[k]);
+                        ++np[k];
                     }
-                    umma_commit(&pv_done[k]);
+                    if (!ok) break;
                     umma_commit(&v_empty[vs]);
-                    ++np[k];
                 }
+                for (int k = 0; k < 2; ++k)
+                    if (U.ntk[k] > 0) ++uo[k];
             }
             if (!ok) s_abort = 1;
             // let every issued MMA finish before the CTA can exit
@@ -339,29 +354,33 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax warpgroups
-        const int k = warp >= 8 ? 1 : 0;
+        const int k = warp >= 8 ? 1 : 0;        // this warpgroup's query tile
         const int row = 32 * (warp & 3) + lane;  // TMEM lane = query row of the tile
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const int wg_tid = threadIdx.x - 128 * (k + 1);
         const uint32_t tS = tbase + lane_off + C::kColS + k * 128;
-        const uint32_t tO = tbase + lane_off + C::kColO;  // O0; O1 follows after D columns
+        const uint32_t tO = tbase + lane_off + C::kColO + k * D;
         const float sl2 = p.scale_log2;
         uint32_t n_s = 0;  // S tiles of this warpgroup (all units)
-        uint32_t kv_it = 0, q_it = 0;
-        for (int u = blockIdx.x; u < num_units && !warp_flag(s_abort); u += gridDim.x, ++q_it) {
+        uint32_t kv_it = 0;
+        for (int u = blockIdx.x; u < num_units && !warp_flag(s_abort); u += gridDim.x) {
             const FaUnit U = fa_unit(p, u);  // the softmax waits for S anyway: no prefetch
-            const int qi = U.row0 + row;  // query index within the request's new tokens
+            const uint32_t kv_base = kv_it;
+            kv_it += U.nkv;
+            const int ntk = k ? U.ntk[1] : U.ntk[0];
+            if (ntk == 0) continue;  // no rows of this unit in this warpgroup's query tile
+            const int row0 = U.row0 + k * BM;
+            const int qi = row0 + row;  // query index within the request's new tokens
+            const int c1 = k ? U.c1k[1] : U.c1k[0];
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
-            const uint32_t kv_base = kv_it;
-            for (int t = k; t < U.ntiles; t += 2) {
+            for (int t = 0; t < ntk; ++t) {
                 if (!mbar_wait_warp(&s_full[k], n_s & 1, p.err)) { ok = false; break; }
                 tc_fence_after();
                 const int kb = U.kb0 + t * BN;
-                const bool edge = (U.slot == 0) ? (kb + BN - 1 > U.row0 || kb + BN > U.c1)
-                                                : (kb < U.c0 || kb + BN > U.c1);
+                const bool edge = (U.slot == 0) ? (kb + BN - 1 > row0 || kb + BN > c1) : (kb < U.c0 || kb + BN > c1);
                 const int lo = U.c0 - kb;  // visible columns: [lo, hi)
-                const int hi = ((U.slot == 0) ? min(qi + 1, U.c1) : U.c1) - kb;
+                const int hi = ((U.slot == 0) ? min(qi + 1, c1) : c1) - kb;
                 // Pass 1: row max of the raw scores (8 independent chains). Pass 2:
                 // P = exp2(scale * s - m_used) as bf16 pairs, written over S_k's
                 // already-read columns (keys 32h.. land in columns 16h..). The body
@@ -390,7 +409,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
                                            fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
                     const float m_new = fmaxf(m_used, mx * sl2);
-                    if (t == k) {
+                    if (t == 0) {
                         m_used = m_new;
                     } else if (m_new > m_used + 8.f) {
                         alpha = fast_exp2(m_used - m_new);
@@ -432,17 +451,19 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
 #pragma unroll 1
                     for (int c = 0; c < D / 16; ++c) {
                         uint32_t r[16];
-                        tmem_ld16(tO + k * D + c * 16, r);
+                        tmem_ld16(tO + c * 16, r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st16(tO + k * D + c * 16, r);
+                        tmem_st16(tO + c * 16, r);
                     }
                 }
                 tmem_wait_st();
                 // last tile of a context chunk: value rows past the chunk end may
-                // hold anything (other positions, NaN-poisoned slots): zero them
-                if (U.slot != 0 && kb + BN > U.c1) {
+                // hold anything (other positions, NaN-poisoned slots): zero them.
+                // Warpgroup 0 does it (it reads every tile of a context chunk);
+                // warpgroup 1's product of the same tile is issued after 0's.
+                if (k == 0 && U.slot != 0 && kb + BN > U.c1) {
                     const uint32_t vi = kv_base + t;
                     if (!mbar_wait_warp(&v_full[vi & 1], (vi >> 1) & 1, p.err)) { ok = false; break; }
                     const int valid = U.c1 - kb;
@@ -459,79 +480,54 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 if (lane == 0) mbar_arrive(&p_full[k]);
                 ++n_s;
             }
-            kv_it = kv_base + U.ntiles;
             if (!ok) {
                 s_abort = 1;
                 break;
             }
-            // ---- epilogue: merge the two warpgroups' (max, sum, O) like two KV splits
-            const FaUnit E = fa_unit(p, u);  // re-read rather than kept live through the tile loop
-            const int n_mine = (E.ntiles - k + 1) / 2, n_other = (E.ntiles - (1 - k) + 1) / 2;
-            if (n_mine > 0 && !mbar_wait_warp(&pv_done[k], (n_s - 1) & 1, p.err)) {
-                s_abort = 1;
-                break;
-            }
-            s_ml[q_it & 1][k][row] = make_float2(m_used, l);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ml_ready);
-            if (!mbar_wait_warp(ml_ready, q_it & 1, p.err)) {
+            // ---- epilogue: O_k row / l once this warpgroup's last P . V is done
+            if (!mbar_wait_warp(&pv_done[k], (n_s - 1) & 1, p.err)) {
                 s_abort = 1;
                 break;
             }
             tc_fence_after();
-            const float2 mo = s_ml[q_it & 1][1 - k][row];
-            const float m = fmaxf(m_used, mo.x);
-            const float f_me = n_mine > 0 ? fast_exp2(m_used - m) : 0.f;
-            const float f_ot = n_other > 0 ? fast_exp2(mo.x - m) : 0.f;
-            const float L = f_me * l + f_ot * mo.y;
-            const float inv = 1.f / L;
-            const float a_me = f_me * inv, a_ot = f_ot * inv;
-            const bool write = qi < E.qlen;
-            const bool final_out = E.slot == 0 && E.ctx == 0;
-            const int64_t orow = final_out ? ((int64_t)(E.q0 + qi) * p.Hq + E.h)
-                                           : (((int64_t)p.ext_base[E.r - p.num_decodes] + (int64_t)E.slot * E.qlen + qi) *
-                                                  p.Hq + E.h);
-            // this warpgroup writes columns [k D/2, (k+1) D/2) of the row: read and
-            // combine both accumulators' halves, release O, then store
-            constexpr int kHalf = D / 2;
-            float o[kHalf];
-#pragma unroll
-            for (int c = 0; c < kHalf / 32; ++c) {
-                const int col0 = k * kHalf + c * 32;
-                uint32_t ra[32], rb[32];
-                if (n_mine > 0) tmem_ld32(tO + k * D + col0, ra);
-                if (n_other > 0) tmem_ld32(tO + (1 - k) * D + col0, rb);
+            const bool write = qi < U.qlen;
+            const bool final_out = U.slot == 0 && U.ctx == 0;
+            const int64_t orow = final_out ? ((int64_t)(U.q0 + qi) * p.Hq + U.h)
+                                           : (((int64_t)p.ext_base[U.r - p.num_decodes] + (int64_t)U.slot * U.qlen + qi) *
+                                                  p.Hq + U.h);
+            const float inv = 1.f / l;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tO + c * 32, r);
                 tmem_wait_ld();
+                if (write) {
+                    if (final_out) {
+                        __nv_bfloat16* dst = p.out + orow * D + c * 32;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    o[c * 32 + i] = (n_mine > 0 ? a_me * __uint_as_float(ra[i]) : 0.f) +
-                                    (n_other > 0 ? a_ot * __uint_as_float(rb[i]) : 0.f);
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 v;
+                            v.x = pack_bf16(__uint_as_float(r[j * 8 + 0]) * inv, __uint_as_float(r[j * 8 + 1]) * inv);
+                            v.y = pack_bf16(__uint_as_float(r[j * 8 + 2]) * inv, __uint_as_float(r[j * 8 + 3]) * inv);
+                            v.z = pack_bf16(__uint_as_float(r[j * 8 + 4]) * inv, __uint_as_float(r[j * 8 + 5]) * inv);
+                            v.w = pack_bf16(__uint_as_float(r[j * 8 + 6]) * inv, __uint_as_float(r[j * 8 + 7]) * inv);
+                            *reinterpret_cast<uint4*>(dst + j * 8) = v;
+                        }
+                    } else {
+                        float* dst = p.ext_o + orow * D + c * 32;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4*>(dst + j * 4) =
+                                make_float4(__uint_as_float(r[j * 4]) * inv, __uint_as_float(r[j * 4 + 1]) * inv,
+                                            __uint_as_float(r[j * 4 + 2]) * inv, __uint_as_float(r[j * 4 + 3]) * inv);
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(o_free);
+            if (lane == 0) mbar_arrive(&o_free[k]);
             if (write) {
-                if (final_out) {
-                    __nv_bfloat16* dst = p.out + orow * D + k * kHalf;
-#pragma unroll
-                    for (int j = 0; j < kHalf / 8; ++j) {
-                        uint4 v;
-                        v.x = pack_bf16(o[j * 8 + 0], o[j * 8 + 1]);
-                        v.y = pack_bf16(o[j * 8 + 2], o[j * 8 + 3]);
-                        v.z = pack_bf16(o[j * 8 + 4], o[j * 8 + 5]);
-                        v.w = pack_bf16(o[j * 8 + 6], o[j * 8 + 7]);
-                        *reinterpret_cast<uint4*>(dst + j * 8) = v;
-                    }
-                } else {
-                    float* dst = p.ext_o + orow * D + k * kHalf;
-#pragma unroll
-                    for (int j = 0; j < kHalf / 4; ++j)
-                        *reinterpret_cast<float4*>(dst + j * 4) = make_float4(o[j * 4], o[j * 4 + 1], o[j * 4 + 2], o[j * 4 + 3]);
-                }
-            }
-            if (write && k == 0) {
-                const float lse_nat = (m + __log2f(L)) * 0.69314718055994531f;
+                const float lse_nat = (m_used + __log2f(l)) * 0.69314718055994531f;
                 if (final_out) {
                     if (p.lse) p.lse[orow] = lse_nat;
                 } else {

@@ -6,7 +6,7 @@
 //
 //   decode:  pairs (request, split) of `dec_split_len` keys each; a unit is a
 //            pair times one KV head (GQA) or one head group (MLA).
-//   prefill/extend: items (request, query tile, slot); slot 0 is the new
+//   prefill/extend: items (request, pair of query tiles, slot); slot 0 is the new
 //            tokens over their own keys (causal), slot c >= 1 is context chunk
 //            c - 1 (the pages' chunked-context loop, run as independent
 //            items); a unit is an item times one query head. Items are
@@ -20,7 +20,9 @@ namespace pka {
 
 constexpr int kMaxRequests = 4096;     // planner keeps per-request metadata in smem
 constexpr int kDecodeMinSplit = 256;   // fewest keys per GQA decode split
-constexpr int kFaBlockM = 128;         // query rows per prefill/extend item (TMEM lanes)
+constexpr int kFaBlockM = 128;         // query rows per prefill/extend query tile (TMEM lanes)
+constexpr int kFaItemTiles = 2;        // query tiles per prefill/extend item
+constexpr int kFaItemRows = kFaBlockM * kFaItemTiles;
 constexpr int kFaBlockN = 128;         // keys per prefill/extend tile (cost unit)
 constexpr int kCostBuckets = 1024;
 
@@ -57,7 +59,7 @@ struct PlanParams {
     int2* dec_pairs;
     int32_t* dec_first;
     int32_t* dec_nsplit;
-    int4* fa_items;      // (request, query tile, slot, cost)
+    int4* fa_items;      // (request, pair of query tiles, slot, cost)
     int32_t* ext_base;   // per extend request: first partial row
 };
 

@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
     }
 
     // ---- prefill / extend items. A group is one (request, slot): all query
-    // tiles that read the same keys. Groups are counting-sorted by the cost of
+    // tiles that read the same keys, taken two by two as items. Groups are counting-sorted by the cost of
     // their heaviest tile (heaviest first) and keep their tiles contiguous, so
     // the CTAs that share a context chunk stream it through L2 together.
     auto group_cost = [&](int r, int slot) -> int {
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
     for (int r = nd + tid; r < B; r += nthr) {
         const int ql = s_qlen[r];
         const int ctx = s_slen[r] - ql;
-        const int nqt = (ql + kFaBlockM - 1) / kFaBlockM;
+        const int nqt = (ql + kFaItemRows - 1) / kFaItemRows;  // items (query-tile pairs)
         const int nslot = (r < nd + ne) ? 1 + (ctx + p.chunk - 1) / p.chunk : 1;
         for (int s = 0; s < nslot; ++s) atomicAdd(&s_hist[group_cost(r, s)], nqt);
     }
@@ -165,12 +165,12 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
     for (int r = nd + tid; r < B; r += nthr) {
         const int ql = s_qlen[r];
         const int ctx = s_slen[r] - ql;
-        const int nqt = (ql + kFaBlockM - 1) / kFaBlockM;
+        const int nqt = (ql + kFaItemRows - 1) / kFaItemRows;  // items (query-tile pairs)
         const int nslot = (r < nd + ne) ? 1 + (ctx + p.chunk - 1) / p.chunk : 1;
         for (int s = 0; s < nslot; ++s) {
             const int c = group_cost(r, s);
             const int pos = atomicAdd(&s_hist[c], nqt);
-            // causal groups: heaviest (last) query tile first
+            // causal groups: heaviest (last) item first
             for (int qt = 0; qt < nqt; ++qt) p.fa_items[pos + qt] = make_int4(r, s == 0 ? nqt - 1 - qt : qt, s, c);
         }
     }
