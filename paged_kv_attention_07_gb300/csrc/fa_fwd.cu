@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 const int hi = ((U.slot == 0) ? min(qi + 1, c1) : c1) - kb;
                 // Pass 1: row max of the raw scores (8 independent chains). Pass 2:
                 // P = exp2(scale * s - m_used) as bf16 pairs, written over S_k's
-                // already-read columns (keys 32h.. land in columns 16h..). The body
+                // already-read columns (keys 64h.. land in columns 32h..). The body
                 // is specialised on whether the tile needs a mask at all (a
                 // per-element mask costs ALU issue slots on every tile otherwise).
                 float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -395,14 +395,15 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
 #pragma unroll
                     for (int j = 0; j < 8; ++j) mxv[j] = -INFINITY;
 #pragma unroll 1
-                    for (int h = 0; h < 4; ++h) {
-                        uint32_t r[32];
-                        tmem_ld32(tS + 32 * h, r);
+                    for (int h = 0; h < 2; ++h) {  // 64 columns per TMEM round trip
+                        uint32_t r[64];
+                        tmem_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(r));
+                        tmem_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
+                        for (int i = 0; i < 64; ++i) {
                             float v = __uint_as_float(r[i]);
-                            if (kMasked && (unsigned)(32 * h + i - lo) >= (unsigned)(hi - lo)) v = -INFINITY;
+                            if (kMasked && (unsigned)(64 * h + i - lo) >= (unsigned)(hi - lo)) v = -INFINITY;
                             mxv[i & 7] = fmaxf(mxv[i & 7], v);
                         }
                     }
@@ -419,25 +420,27 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     }
                     const float m_off = m_used == -INFINITY ? 0.f : m_used;
 #pragma unroll 1
-                    for (int h = 0; h < 4; ++h) {
-                        uint32_t r[32];
-                        tmem_ld32(tS + 32 * h, r);
+                    for (int h = 0; h < 2; ++h) {  // 64 columns per TMEM round trip
+                        uint32_t r[64];
+                        tmem_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(r));
+                        tmem_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
                         tmem_wait_ld();
-                        uint32_t pk[16];
+                        uint32_t pk[32];
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
+                        for (int i = 0; i < 64; i += 2) {
                             float v0 = __uint_as_float(r[i]);
                             float v1 = __uint_as_float(r[i + 1]);
                             if (kMasked) {
-                                if ((unsigned)(32 * h + i - lo) >= (unsigned)(hi - lo)) v0 = -INFINITY;
-                                if ((unsigned)(32 * h + i + 1 - lo) >= (unsigned)(hi - lo)) v1 = -INFINITY;
+                                if ((unsigned)(64 * h + i - lo) >= (unsigned)(hi - lo)) v0 = -INFINITY;
+                                if ((unsigned)(64 * h + i + 1 - lo) >= (unsigned)(hi - lo)) v1 = -INFINITY;
                             }
                             const float e0 = fast_exp2(fmaf(v0, sl2, -m_off));
                             const float e1 = fast_exp2(fmaf(v1, sl2, -m_off));
                             ls[(i >> 1) & 7] += e0 + e1;
                             pk[i / 2] = pack_bf16(e0, e1);
                         }
-                        tmem_st16(tS + 16 * h, pk);
+                        // keys 64h.. land in P columns 32h.. (S columns already read)
+                        tmem_st32(tS + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(pk));
                     }
                 };
                 if (edge) tile_body(std::true_type{});
