@@ -235,7 +235,7 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
     # (name, spec, dominant kernel, bound, L2 flush bytes, committed ncu traffic entry)
     cases = [("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20,
               ("fa_fwd.cu", "fa_fwd_prefill_varlen")),
-             ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0, None),
+             ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0, ("fa_fwd.cu", "fa_fwd_mixed")),
              ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0,
               ("decode_mla_tc.cu", "decode_mla_tc_mla_decode_bs64")),
              ("mla_decode_bs1", W.spec_mla_decode(block_size=1), "decode", "hbm", 0, None)]
