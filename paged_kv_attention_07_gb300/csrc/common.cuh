@@ -93,6 +93,21 @@ PKA_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
     }
 }
 
+// Bounded wait until a monotonic shared-memory counter reaches `target`
+// (written by another thread of the CTA). Returns false (and sets the
+// timeout bit) if it did not within kWaitLimitNs.
+PKA_DEVICE bool wait_counter(const volatile int& counter, int target, int32_t* err) {
+    if (counter >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (counter >= target) return true;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+            set_error(err, PKA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Full-warp forms: every lane of the warp gets the same answer, so a timeout
 // or an abort can never split a warp at a later warp-synchronous point
 // (__syncwarp, shuffles, .sync.aligned instructions). Call with all 32 lanes.

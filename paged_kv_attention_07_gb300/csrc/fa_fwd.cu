@@ -135,6 +135,11 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
     uint64_t* o_free = bars + 16;    // [2] its epilogue has read O_k (4 warp arrivals)
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
+    // Key tiles (global count) after which the S issuer has issued query tile
+    // 0's next S: the P . V issuer lets query tile 1's product of tile g go
+    // only once this exceeds g, so the tensor pipe runs P_0 V, S_0 (next),
+    // P_1 V, S_1 (next) and warpgroup 0 never queues behind warpgroup 1.
+    __shared__ volatile int s_qk0_next;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_units = p.hdr->fa_num_items * p.Hq;
@@ -155,6 +160,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         }
         fence_barrier_init();
         s_abort = 0;
+        s_qk0_next = 0;
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.knew);
         tma_prefetch_desc(&maps.vnew);
@@ -288,6 +294,9 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 for (int t = 0; t < U.nkv; ++t, ++kv_it) {
                     const int st = kv_it & 1;
                     if (!mbar_wait(&k_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                    // query tile 0 has no S of this tile: tile 1's product of the
+                    // previous tile may go now (its next S below waits for it)
+                    if (t > 0 && t >= U.ntk[0]) s_qk0_next = (int)kv_it;
                     for (int k = 0; k < 2; ++k) {
                         if (t >= U.ntk[k]) continue;
                         if (nq[k] > 0 && !mbar_wait(&pv_done[k], (nq[k] - 1) & 1, p.err)) { ok = false; break; }
@@ -302,11 +311,15 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                         }
                         umma_commit(&s_full[k]);
                         ++nq[k];
+                        // query tile 0's S of this tile is issued: query tile 1's
+                        // product of the previous tile may go
+                        if (k == 0 && t > 0) s_qk0_next = (int)kv_it;
                     }
                     if (!ok) break;
                     umma_commit(&k_empty[st]);
                     if (t == U.nkv - 1) umma_commit(q_empty);
                 }
+                if (ok) s_qk0_next = (int)kv_it;  // the unit's last tile: nothing of query tile 0 follows
             }
             if (!ok) s_abort = 1;
             for (int k = 0; k < 2; ++k)
@@ -327,6 +340,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     if (!mbar_wait(&v_full[vs], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
                     for (int k = 0; k < 2; ++k) {
                         if (t >= U.ntk[k]) continue;
+                        if (k == 1 && !wait_counter(s_qk0_next, (int)kv_it + 1, p.err)) { ok = false; break; }
                         if (!mbar_wait(&p_full[k], np[k] & 1, p.err)) { ok = false; break; }
                         // a unit's first product overwrites O_k: its previous epilogue must have read it
                         if (t == 0 && uo[k] > 0 && !mbar_wait(&o_free[k], (uo[k] - 1) & 1, p.err)) { ok = false; break; }
