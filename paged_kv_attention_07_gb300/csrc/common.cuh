@@ -1,7 +1,7 @@
 // common.cuh -- device helpers shared by the kernels of libpka.so (sm_103a).
 //
-// Inline PTX for the pieces the kernels are built from: mbarrier waits with a
-// bounded spin, TMA tile loads, cp.async with mbarrier completion,
+// Inline PTX for the pieces the kernels are built from: bounded mbarrier
+// waits (the waiting thread sleeps), TMA tile loads, cp.async with mbarrier completion,
 // ldmatrix/movmatrix, bf16 tensor-core MMA, and bf16 packing.
 #pragma once
 
@@ -20,6 +20,9 @@ namespace pka {
 // records PKA_DEVERR_TIMEOUT and lets the kernel finish without touching
 // the stage it waited for. Nothing here should ever take a millisecond.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Longest single suspension inside an mbarrier wait (the thread wakes as soon
+// as the phase completes; this only bounds how late a timeout is noticed).
+constexpr uint32_t kSuspendNs = 1000000u;  // 1 ms
 
 PKA_DEVICE uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -54,14 +57,16 @@ PKA_DEVICE void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-PKA_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Blocking probe: the thread is suspended (it takes no issue slots) until the
+// phase completes or about `suspend_ns` pass, whichever comes first.
+PKA_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
@@ -82,11 +87,14 @@ PKA_DEVICE bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // timeout bit) if the phase did not complete within kWaitLimitNs.
 PKA_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
     if (mbar_test_wait(bar, parity)) return true;  // non-blocking fast path
-    if (mbar_try_wait(bar, parity)) return true;
+    // A waiting thread sleeps inside try_wait instead of spinning: a spinning
+    // warp would take issue slots from the warps of the same scheduler that
+    // have work (the softmax warps share schedulers with the copy and MMA
+    // warps, and with each other).
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    for (;;) {
+        if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
             set_error(err, PKA_DEVERR_TIMEOUT);
             return false;
         }
@@ -264,6 +272,32 @@ PKA_DEVICE uint32_t pack_bf16(float lo, float hi) {
 
 PKA_DEVICE float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 PKA_DEVICE float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// max(a, b, c) in one instruction (three-input max, sm_100 and later).
+PKA_DEVICE float fmax3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (d0, d1) = (a0 * b + c, a1 * b + c): one packed fp32 FMA, each lane rounded
+// like fmaf.
+PKA_DEVICE void fma2_bcast(float& d0, float& d1, float a0, float a1, float b, float c) {
+    asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+        "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\tmov.b64 z, {%5, %5};\n\t"
+        "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1): one packed fp32 add.
+PKA_DEVICE void add2(float& s0, float& s1, float a0, float a1) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+        "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a0), "f"(a1));
+}
 
 PKA_DEVICE float fast_exp2(float x) {
     float y;

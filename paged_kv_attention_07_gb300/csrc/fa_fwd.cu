@@ -395,16 +395,52 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 const bool edge = (U.slot == 0) ? (kb + BN - 1 > row0 || kb + BN > c1) : (kb < U.c0 || kb + BN > c1);
                 const int lo = U.c0 - kb;  // visible columns: [lo, hi)
                 const int hi = ((U.slot == 0) ? min(qi + 1, c1) : c1) - kb;
-                // Pass 1: row max of the raw scores (8 independent chains). Pass 2:
-                // P = exp2(scale * s - m_used) as bf16 pairs, written over S_k's
-                // already-read columns (keys 64h.. land in columns 32h..). The body
-                // is specialised on whether the tile needs a mask at all (a
-                // per-element mask costs ALU issue slots on every tile otherwise).
+                // General body, two passes over S_k in TMEM. Pass 1: row max of the
+                // raw scores (8 independent chains). Pass 2: P = exp2(scale * s -
+                // m_used) as bf16 pairs, written over S_k's already-read columns
+                // (keys 64h.. land in columns 32h..). Specialised on whether the
+                // tile needs a mask at all (a per-element mask costs ALU issue
+                // slots on every tile otherwise).
                 float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 bool rescale = false;
                 float alpha = 1.f;
-                auto tile_body = [&](auto masked_c) {
+                // exponentials of 64 scores (one TMEM round trip) into bf16 pairs
+                auto exp_half = [&](const uint32_t (&r)[64], uint32_t (&pk)[32], float m_off, auto masked_c, int h) {
                     constexpr bool kMasked = decltype(masked_c)::value;
+#pragma unroll
+                    for (int i = 0; i < 64; i += 2) {
+                        float v0 = __uint_as_float(r[i]);
+                        float v1 = __uint_as_float(r[i + 1]);
+                        if (kMasked) {
+                            if ((unsigned)(64 * h + i - lo) >= (unsigned)(hi - lo)) v0 = -INFINITY;
+                            if ((unsigned)(64 * h + i + 1 - lo) >= (unsigned)(hi - lo)) v1 = -INFINITY;
+                        }
+                        float x0, x1;
+                        fma2_bcast(x0, x1, v0, v1, sl2, -m_off);
+                        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                        const int j = (i >> 1) & 3;
+                        add2(ls[2 * j], ls[2 * j + 1], e0, e1);
+                        pk[i / 2] = pack_bf16(e0, e1);
+                    }
+                };
+                auto max_half = [&](const uint32_t (&r)[64], float (&mxv)[8], auto masked_c, int h) {
+                    constexpr bool kMasked = decltype(masked_c)::value;
+#pragma unroll
+                    for (int i = 0; i < 64; i += 2) {
+                        float v0 = __uint_as_float(r[i]);
+                        float v1 = __uint_as_float(r[i + 1]);
+                        if (kMasked) {
+                            if ((unsigned)(64 * h + i - lo) >= (unsigned)(hi - lo)) v0 = -INFINITY;
+                            if ((unsigned)(64 * h + i + 1 - lo) >= (unsigned)(hi - lo)) v1 = -INFINITY;
+                        }
+                        mxv[(i >> 1) & 7] = fmax3f(mxv[(i >> 1) & 7], v0, v1);
+                    }
+                };
+                auto reduce8 = [](const float (&mxv)[8]) {
+                    return fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                                 fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
+                };
+                auto tile_body = [&](auto masked_c) {
                     float mxv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) mxv[j] = -INFINITY;
@@ -414,16 +450,9 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                         tmem_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(r));
                         tmem_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
                         tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) {
-                            float v = __uint_as_float(r[i]);
-                            if (kMasked && (unsigned)(64 * h + i - lo) >= (unsigned)(hi - lo)) v = -INFINITY;
-                            mxv[i & 7] = fmaxf(mxv[i & 7], v);
-                        }
+                        max_half(r, mxv, masked_c, h);
                     }
-                    const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
-                                           fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
-                    const float m_new = fmaxf(m_used, mx * sl2);
+                    const float m_new = fmaxf(m_used, reduce8(mxv) * sl2);
                     if (t == 0) {
                         m_used = m_new;
                     } else if (m_new > m_used + 8.f) {
@@ -440,25 +469,59 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                         tmem_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
                         tmem_wait_ld();
                         uint32_t pk[32];
-#pragma unroll
-                        for (int i = 0; i < 64; i += 2) {
-                            float v0 = __uint_as_float(r[i]);
-                            float v1 = __uint_as_float(r[i + 1]);
-                            if (kMasked) {
-                                if ((unsigned)(64 * h + i - lo) >= (unsigned)(hi - lo)) v0 = -INFINITY;
-                                if ((unsigned)(64 * h + i + 1 - lo) >= (unsigned)(hi - lo)) v1 = -INFINITY;
-                            }
-                            const float e0 = fast_exp2(fmaf(v0, sl2, -m_off));
-                            const float e1 = fast_exp2(fmaf(v1, sl2, -m_off));
-                            ls[(i >> 1) & 7] += e0 + e1;
-                            pk[i / 2] = pack_bf16(e0, e1);
-                        }
+                        exp_half(r, pk, m_off, masked_c, h);
                         // keys 64h.. land in P columns 32h.. (S columns already read)
                         tmem_st32(tS + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(pk));
                     }
                 };
-                if (edge) tile_body(std::true_type{});
-                else tile_body(std::false_type{});
+                // Common case, one pass: an unmasked tile after the row's first,
+                // whose scores stay within the lazy-rescale margin of m_used, gets
+                // its exponentials as each half is read. Half 0's P stays in
+                // registers until half 1's max is known, so S_k is intact in TMEM
+                // when a row of the warp turns out to need more (then the general
+                // body runs from the start; the choice is warp-uniform because
+                // tcgen05.ld/st are warp-collective).
+                auto tile_fast = [&]() -> bool {
+                    uint32_t pk0[32];
+                    {
+                        uint32_t r[64];
+                        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(r));
+                        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                        tmem_wait_ld();
+                        float mxv[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) mxv[j] = -INFINITY;
+                        max_half(r, mxv, std::false_type{}, 0);
+                        if (__any_sync(0xffffffffu, reduce8(mxv) * sl2 > m_used + 8.f)) return false;
+                        exp_half(r, pk0, m_used, std::false_type{}, 0);
+                    }
+                    uint32_t r[64];
+                    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+                    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                    tmem_wait_ld();
+                    float mxv[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) mxv[j] = -INFINITY;
+                    max_half(r, mxv, std::false_type{}, 1);
+                    if (__any_sync(0xffffffffu, reduce8(mxv) * sl2 > m_used + 8.f)) return false;
+                    tmem_st32(tS, pk0);  // keys 0..63 -> P columns 0..31 (S columns 0..63 were read)
+                    uint32_t pk[32];
+                    exp_half(r, pk, m_used, std::false_type{}, 1);
+                    tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                    return true;
+                };
+                bool done = false;
+                if (!edge && t > 0) {
+                    done = tile_fast();
+                    if (!done) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) ls[j] = 0.f;
+                    }
+                }
+                if (!done) {
+                    if (edge) tile_body(std::true_type{});
+                    else tile_body(std::false_type{});
+                }
                 l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 // O_k's previous product finished before this S tile was computed.
                 // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
