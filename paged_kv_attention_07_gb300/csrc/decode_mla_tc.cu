@@ -26,9 +26,10 @@
 // partial tile, whose missing rows are zero-filled).
 //
 // Persistent CTAs, one per SM, allocate tensor memory once and take units
-// from an atomic counter; the producer publishes each unit index to the other
-// roles through a 2-slot ring in shared memory. Warps: 0 producer, 1 tensor-
-// memory owner + MMA issuer (one thread), 2-5 softmax (one thread per head):
+// from an atomic counter; warp 0 publishes each unit index to the other roles
+// through a 2-slot ring in shared memory. Warps: 0 producer of q and the
+// score-only chunks, 6 producer of the value chunks, 1 tensor-memory owner +
+// MMA issuer (one thread), 2-5 softmax (one thread per head):
 // S row -> online softmax (the O rescale is lazy: only when the max grew by
 // more than 2^8) -> P into TMEM; at the end of a unit O / l goes to out, or
 // to the fp32 split partials + LSE that the decode reduction merges.
@@ -41,9 +42,8 @@
 
 namespace pka {
 
-constexpr int kMtThreads = 192;
+constexpr int kMtThreads = 224;
 constexpr int kMtTile = 64;                       // keys per tile (the N of S)
-constexpr int kMtPrefetch = 2;                    // tiles of L2 prefetch ahead of the copies
 constexpr int kMtD = 576, kMtDv = 512, kMtHalf = 256;
 constexpr int kMtQtDims = 320;                    // q dims held in TMEM
 constexpr int kMtChunk = kMtTile * 128;           // one 64-dim column chunk of a tile (8 KB)
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     uint64_t* kv_full_v = bars + 16;  // [2] value chunks landed
     uint64_t* kv_empty_v = bars + 18; // [2] value chunks read by S and P . V
     uint64_t* u_full = bars + 4;     // [2] unit ring slot written
-    uint64_t* u_empty = bars + 6;    // [2] unit ring slot read by the issuer and the 4 softmax warps
+    uint64_t* u_empty = bars + 6;    // [2] unit ring slot read by the issuer, the value producer and the 4 softmax warps
     uint64_t* q_full = bars + 8;     // q[:, 320:576] landed in shared memory
     uint64_t* q_empty = bars + 9;    // the unit's last S product is done (Q free again)
     uint64_t* qt_ready = bars + 10;  // q[:, 0:320] written to TMEM (4 warps)
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             mbar_init(&kv_full_v[i], 1);
             mbar_init(&kv_empty_v[i], 1);
             mbar_init(&u_full[i], 1);
-            mbar_init(&u_empty[i], 5);
+            mbar_init(&u_empty[i], 6);
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
@@ -151,44 +151,55 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         return true;
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 6) {
+        // ------------------------------------------------------------ producers
+        // warp 0 takes the units and loads q[:, 320:576] and the score-only
+        // part of each stage; warp 6 loads the value part, so neither part of
+        // a stage waits behind the other's free slot.
+        const int part = warp == 6 ? 1 : 0;
         const uint64_t pol = policy_evict_normal();  // the other value half re-reads each tile
         const bool use_tma = p.bs >= 8;
         uint32_t kv_it = 0, q_it = 0;
-        uint32_t last[2] = {0, 0};  // phase + 1 of the last copy per stage (0 = none)
+        uint32_t last[2] = {0, 0};  // phase + 1 of this part's last copy per stage (0 = none)
         for (uint32_t i = 0; !warp_flag(s_abort); ++i) {
-            const int slot = i & 1;
-            if (i >= 2 && !mbar_wait_warp(&u_empty[slot], ((i >> 1) - 1) & 1, p.err)) {
+            int u = 0;
+            if (part == 0) {
+                const int slot = i & 1;
+                if (i >= 2 && !mbar_wait_warp(&u_empty[slot], ((i >> 1) - 1) & 1, p.err)) {
+                    s_abort = 1;
+                    break;
+                }
+                if (lane == 0) u = atomicAdd(p.counter, 1);
+                u = __shfl_sync(0xffffffffu, u, 0);
+                if (u >= num_units) u = -1;
+                if (lane == 0) {
+                    s_unit[slot] = u;
+                    mbar_arrive(&u_full[slot]);
+                }
+                __syncwarp();
+            } else if (!take_unit(i, lane == 0, &u)) {
                 s_abort = 1;
                 break;
             }
-            int u = 0;
-            if (lane == 0) u = atomicAdd(p.counter, 1);
-            u = __shfl_sync(0xffffffffu, u, 0);
-            if (u >= num_units) u = -1;
-            if (lane == 0) {
-                s_unit[slot] = u;
-                mbar_arrive(&u_full[slot]);
-            }
-            __syncwarp();
             if (u < 0) break;
             const MlaTcUnit U = mla_tc_unit(p, u, L);
             if (!mla_tc_unit_ok(p, U)) {
-                if (lane == 0) set_error(p.err, PKA_DEVERR_CAPACITY);
+                if (part == 0 && lane == 0) set_error(p.err, PKA_DEVERR_CAPACITY);
                 continue;
             }
-            if (q_it > 0 && !mbar_wait_warp(q_empty, (q_it - 1) & 1, p.err)) {
-                s_abort = 1;
-                break;
+            if (part == 0) {
+                if (q_it > 0 && !mbar_wait_warp(q_empty, (q_it - 1) & 1, p.err)) {
+                    s_abort = 1;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full, kMtQsBytes);
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_3d(smem + kMtOffQ + c * kMtQsChunk, &qmap, q_full, kMtQtDims + c * 64, U.grp * 128,
+                                    U.r, pol);
+                }
+                ++q_it;
             }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(q_full, kMtQsBytes);
-                for (int c = 0; c < 4; ++c)
-                    tma_load_3d(smem + kMtOffQ + c * kMtQsChunk, &qmap, q_full, kMtQtDims + c * 64, U.grp * 128, U.r,
-                                pol);
-            }
-            ++q_it;
             const int32_t* bt = p.block_table + (int64_t)U.r * p.max_blocks;
             // validated block id of key position `pos` of this request
             auto block_of = [&](int pos) -> int {
@@ -204,26 +215,6 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
                 const int st = kv_it & 1;
                 const uint32_t n = kv_it >> 1;
-                // L2 prefetch of the tile kMtPrefetch ahead (its stage is still
-                // busy), so the copy that refills a freed stage reads from L2
-                if (t + kMtPrefetch < U.ntiles) {
-                    const int pb = U.k0 + (t + kMtPrefetch) * kMtTile;
-                    const int pv = min(kMtTile, U.k1 - pb);
-                    if (use_tma) {
-                        const int rows = p.bs < kMtTile ? p.bs : kMtTile;
-                        const int nbox = (pv + rows - 1) / rows;
-                        if (lane < nbox) {
-                            const int pos = pb + lane * rows;
-                            const int row = block_of(pos) * p.bs + (pos % p.bs);
-                            for (int c = 0; c < 9; ++c) tma_prefetch_2d(&kvmap, c * 64, row);
-                        }
-                    } else {
-                        for (int r = lane; r < pv; r += 32) {
-                            const int pos = pb + r;
-                            bulk_prefetch_l2(p.kv + ((int64_t)block_of(pos) * p.bs + pos % p.bs) * kMtD, kMtD * 2);
-                        }
-                    }
-                }
                 uint8_t* dst = smem + kMtOffKV + st * kMtTileBytes;
                 const int tb = U.k0 + t * kMtTile;
                 const int valid = min(kMtTile, U.k1 - tb);
@@ -231,7 +222,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 const int blk_lo = (!tma && tb + lane < U.k1) ? block_of(tb + lane) : 0;
                 const int blk_hi = (!tma && tb + 32 + lane < U.k1) ? block_of(tb + 32 + lane) : 0;
                 // part 0: the score-only chunks, part 1: the value chunks
-                for (int part = 0; part < 2; ++part) {
+                {
                     uint64_t* empty = part ? &kv_empty_v[st] : &kv_empty[st];
                     uint64_t* full = part ? &kv_full_v[st] : &kv_full[st];
                     const uint32_t cmask = part ? vmask : (0x1FFu & ~vmask);
@@ -301,10 +292,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         }
         // no copy may outlive the CTA: wait (bounded) for the last one per stage
         for (int st = 0; st < 2; ++st)
-            if (last[st]) {
-                mbar_wait_warp(&kv_full[st], (last[st] - 1) & 1, p.err);
-                mbar_wait_warp(&kv_full_v[st], (last[st] - 1) & 1, p.err);
-            }
+            if (last[st]) mbar_wait_warp(part ? &kv_full_v[st] : &kv_full[st], (last[st] - 1) & 1, p.err);
         if (q_it > 0) mbar_wait_warp(q_full, (q_it - 1) & 1, p.err);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -400,7 +388,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         // let every issued MMA finish before the CTA can exit
         if (lane == 0 && pv_it > 0) mbar_wait(pv_done, (pv_it - 1) & 1, p.err);
         __syncwarp();
-    } else {
+    } else if (warp <= 5) {
         // ------------------------------------------------------------ softmax (one thread per head)
         const int hl = 32 * (warp & 3) + lane;  // head within the group = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
