@@ -273,6 +273,22 @@ PKA_API pka_status pka_kernel_timer(int kernel, int enable);
 /* Summed duration (ms) and launch count of `kernel` since it was enabled. */
 PKA_API pka_status pka_kernel_timer_read(int kernel, double *total_ms, int *launches, int *timed);
 
+/*
+ * pka_selftest_wait -- the library's bounded pipeline wait (the one every
+ * kernel uses between its copy, MMA and softmax roles), run on its own: one
+ * warp waits on a shared-memory mbarrier. With arrive != 0 one of its threads
+ * completes the barrier's phase first and the wait returns at once; with
+ * arrive == 0 nothing ever arrives, so the wait gives up after limit_us
+ * microseconds, records PKA_DEVERR_TIMEOUT in the run's device error word and
+ * the kernel exits normally (the CUDA context stays usable). The run's error
+ * word (0 or PKA_DEVERR_TIMEOUT) is written to *code_out. Synchronises
+ * `stream` (NULL = legacy default stream).
+ * Returns PKA_ERR_INVALID_ARG for a NULL code_out or limit_us outside
+ * [1, 2000000], PKA_ERR_CUDA on a launch or copy failure, else PKA_OK (also
+ * when the wait timed out: that is reported through *code_out).
+ */
+PKA_API pka_status pka_selftest_wait(int arrive, uint32_t limit_us, int32_t *code_out, void *stream);
+
 /* A static, human-readable name of a status. */
 PKA_API const char *pka_status_string(pka_status status);
 

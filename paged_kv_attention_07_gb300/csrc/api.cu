@@ -237,6 +237,28 @@ uint8_t* noalloc_scratch() {
 
 using namespace pka;
 
+namespace pka {
+
+__device__ int32_t g_selftest_err;
+
+// One warp waits on an mbarrier that only it can complete (arrive != 0) or
+// that nothing completes (arrive == 0: the bounded wait runs out).
+__global__ void selftest_wait_kernel(int arrive, uint64_t limit_ns, int32_t* err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (arrive && threadIdx.x == 0) mbar_arrive(&bar);
+    __syncwarp();
+    const bool ok = mbar_wait_limit(&bar, 0, threadIdx.x == 0 ? err : nullptr, limit_ns);
+    __syncwarp();
+    (void)__all_sync(0xffffffffu, ok);
+}
+
+}  // namespace pka
+
 extern "C" {
 
 const char* pka_status_string(pka_status s) {
@@ -728,6 +750,21 @@ pka_status pka_kernel_timer_read(int kernel, double* total_ms, int* launches, in
     if (total_ms) *total_ms = sum;
     if (launches) *launches = t.launches;
     if (timed_out) *timed_out = t.timed;
+    return PKA_OK;
+}
+
+pka_status pka_selftest_wait(int arrive, uint32_t limit_us, int32_t* code_out, void* stream) {
+    if (!code_out || limit_us < 1 || limit_us > 2000000u) return PKA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* d_err = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d_err), pka::g_selftest_err) != cudaSuccess) return PKA_ERR_CUDA;
+    if (cudaMemsetAsync(d_err, 0, sizeof(int32_t), st) != cudaSuccess) return PKA_ERR_CUDA;
+    pka::selftest_wait_kernel<<<1, 32, 0, st>>>(arrive, (uint64_t)limit_us * 1000ull, d_err);
+    if (cudaGetLastError() != cudaSuccess) return PKA_ERR_CUDA;
+    int32_t code = 0;
+    if (cudaMemcpyAsync(&code, d_err, sizeof(code), cudaMemcpyDeviceToHost, st) != cudaSuccess) return PKA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PKA_ERR_CUDA;
+    *code_out = code;
     return PKA_OK;
 }
 

@@ -85,20 +85,25 @@ PKA_DEVICE bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait for phase `parity` of `bar`. Returns false (and sets the
 // timeout bit) if the phase did not complete within kWaitLimitNs.
-PKA_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+PKA_DEVICE bool mbar_wait_limit(uint64_t* bar, uint32_t parity, int32_t* err, uint64_t limit_ns) {
     if (mbar_test_wait(bar, parity)) return true;  // non-blocking fast path
     // A waiting thread sleeps inside try_wait instead of spinning: a spinning
     // warp would take issue slots from the warps of the same scheduler that
     // have work (the softmax warps share schedulers with the copy and MMA
     // warps, and with each other).
     const uint64_t t0 = global_timer_ns();
+    const uint32_t nap = limit_ns < kSuspendNs ? (uint32_t)limit_ns : kSuspendNs;
     for (;;) {
-        if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (mbar_try_wait(bar, parity, nap)) return true;
+        if (global_timer_ns() - t0 > limit_ns) {
             set_error(err, PKA_DEVERR_TIMEOUT);
             return false;
         }
     }
+}
+
+PKA_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+    return mbar_wait_limit(bar, parity, err, kWaitLimitNs);
 }
 
 // Bounded wait until a monotonic shared-memory counter reaches `target`

@@ -20,7 +20,7 @@ DEVERR = {"QUERY_START_LOC": 0x01, "SEQ_LEN": 0x02, "ORDER": 0x04, "QUERY_LEN": 
           "BLOCK_TABLE": 0x10, "BLOCK_ID": 0x20, "SLOT": 0x40, "CAPACITY": 0x80, "TIMEOUT": 0x100}
 EXPORTED = ("pka_cache_write", "pka_workspace_size", "pka_paged_attn_forward",
             "pka_merge_attn_states", "pka_get_error", "pka_paged_decode_noalloc", "pka_kernel_timer",
-            "pka_kernel_timer_read", "pka_status_string")
+            "pka_kernel_timer_read", "pka_selftest_wait", "pka_status_string")
 KERNELS = {"cache_write": 0, "planner": 1, "decode": 2, "decode_reduce": 3, "prefill_extend": 4,
            "extend_reduce": 5, "merge": 6}
 
@@ -69,6 +69,8 @@ def load(path: str | None = None):
     lib.pka_kernel_timer_read.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                                           ctypes.POINTER(ctypes.c_int)]
     lib.pka_status_string.restype = ctypes.c_char_p
+    lib.pka_selftest_wait.argtypes = [i32, ctypes.c_uint32, ctypes.POINTER(ctypes.c_int32), P]
+    lib.pka_selftest_wait.restype = i32
     lib.pka_status_string.argtypes = [i32]
     if path is None:
         _lib = lib
@@ -162,6 +164,15 @@ def pka_kernel_timer_read(kernel: str):
     _check(load().pka_kernel_timer_read(KERNELS[kernel], ctypes.byref(ms), ctypes.byref(n),
                                         ctypes.byref(t)), "pka_kernel_timer_read")
     return float(ms.value), int(n.value), int(t.value)
+
+
+def pka_selftest_wait(arrive: bool, limit_us: int, stream=None) -> int:
+    """Run the library's bounded mbarrier wait alone (see include/pka.h); returns
+    the run's device error word (0, or PKA_DEVERR_TIMEOUT when nothing arrived)."""
+    code = ctypes.c_int32(0)
+    _check(load().pka_selftest_wait(1 if arrive else 0, int(limit_us), ctypes.byref(code),
+                                    _stream(stream)), "pka_selftest_wait")
+    return int(code.value)
 
 
 def pka_status_string(status: int) -> str:

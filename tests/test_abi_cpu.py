@@ -108,3 +108,10 @@ def test_merge_and_get_error_reject_bad_arguments(lib):
 def test_workspace_size_rejects_unsupported_shapes(lib):
     assert lib.pka_workspace_size(1, 0, 0, 1, 4, 2, 96, 96, 1, 10, 32) == 0
     assert lib.pka_workspace_size(1, 0, 0, 1, 6, 4, 64, 64, 1, 10, 32) == 0
+
+
+@pytest.mark.parametrize("limit_us,with_code", [(0, True), (2000001, True), (1000, False)])
+def test_selftest_wait_rejects_bad_arguments(lib, limit_us, with_code):
+    code = ctypes.c_int32(0)
+    st = lib.pka_selftest_wait(0, limit_us, ctypes.byref(code) if with_code else None, None)
+    assert st == 1  # PKA_ERR_INVALID_ARG, before any CUDA call
