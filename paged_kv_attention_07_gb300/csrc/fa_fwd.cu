@@ -20,7 +20,8 @@
 //            sizes below 8 use cp.async copies for K and V);
 //   warp 1   tensor-memory owner; one thread issues S_k = Q_k K^T for both
 //            query tiles k of every K tile;
-//   warp 3   one thread issues O_k += P_k V (A operand P_k read from TMEM);
+//   warp 3   one thread issues O_k += P_k V (A operand P_k read from TMEM),
+//            keys 0..63 first when the softmax signals that half early;
 //   warps 4-7, 8-11: softmax warpgroup k owns query tile k, one thread per
 //            query row (= TMEM lane), with its own S_k, running max and sum
 //            and O_k. Each reads its S row twice (row max, then exponentials:
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
     uint64_t* p_full = bars + 12;    // [2] its P is in TMEM (4 warp arrivals)
     uint64_t* pv_done = bars + 14;   // [2] the P . V that read its P is done
     uint64_t* o_free = bars + 16;    // [2] its epilogue has read O_k (4 warp arrivals)
+    uint64_t* p_half = bars + 18;    // [2] the first half of its P (keys 0..63) is in TMEM (4 warp arrivals)
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     // Key tiles (global count) after which the S issuer has issued query tile
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
+            mbar_init(&p_half[i], 4);
             mbar_init(&pv_done[i], 1);
             mbar_init(&o_free[i], 4);
         }
@@ -341,17 +344,27 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     for (int k = 0; k < 2; ++k) {
                         if (t >= U.ntk[k]) continue;
                         if (k == 1 && !wait_counter(s_qk0_next, (int)kv_it + 1, p.err)) { ok = false; break; }
-                        if (!mbar_wait(&p_full[k], np[k] & 1, p.err)) { ok = false; break; }
-                        // a unit's first product overwrites O_k: its previous epilogue must have read it
-                        if (t == 0 && uo[k] > 0 && !mbar_wait(&o_free[k], (uo[k] - 1) & 1, p.err)) { ok = false; break; }
-                        tc_fence_after();
+                        // keys 0..63 of P may be stored before the rest (the softmax's
+                        // one-pass tiles signal them early): their half of the product
+                        // goes first
+                        for (int hh = 0; hh < 2 && ok; ++hh) {
+                            if (!mbar_wait(hh ? &p_full[k] : &p_half[k], np[k] & 1, p.err)) { ok = false; break; }
+                            // a unit's first product overwrites O_k: its previous epilogue must have read it
+                            if (hh == 0 && t == 0 && uo[k] > 0 && !mbar_wait(&o_free[k], (uo[k] - 1) & 1, p.err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            const uint64_t bdesc =
-                                umma_desc_sw128(v_s + vs * C::kKVBytes + kk * 2048, C::kChunkBytes, 1024);
-                            umma_bf16_ts(tbase + C::kColO + k * D, tbase + C::kColS + k * 128 + kk * 8, bdesc,
-                                         idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                            for (int kq = 0; kq < BN / 32; ++kq) {
+                                const int kk = hh * (BN / 32) + kq;
+                                const uint64_t bdesc =
+                                    umma_desc_sw128(v_s + vs * C::kKVBytes + kk * 2048, C::kChunkBytes, 1024);
+                                umma_bf16_ts(tbase + C::kColO + k * D, tbase + C::kColS + k * 128 + kk * 8, bdesc,
+                                             idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                            }
                         }
+                        if (!ok) break;
                         umma_commit(&pv_done[k]);
                         ++np[k];
                     }
@@ -505,6 +518,12 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     max_half(r, mxv, std::false_type{}, 1);
                     if (__any_sync(0xffffffffu, reduce8(mxv) * sl2 > m_used + 8.f)) return false;
                     tmem_st32(tS, pk0);  // keys 0..63 -> P columns 0..31 (S columns 0..63 were read)
+                    // their half of P . V may start while the rest is computed (no
+                    // rescale on this path, and no V rows to zero: both need a mask)
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_half[k]);
                     uint32_t pk[32];
                     exp_half(r, pk, m_used, std::false_type{}, 1);
                     tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk));
@@ -557,7 +576,10 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[k]);
+                if (lane == 0) {
+                    if (!done) mbar_arrive(&p_half[k]);
+                    mbar_arrive(&p_full[k]);
+                }
                 ++n_s;
             }
             if (!ok) {
