@@ -522,6 +522,7 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
         fp.ext_o = reinterpret_cast<float*>(ws + L.off_ext_part_o);
         fp.ext_lse = reinterpret_cast<float*>(ws + L.off_ext_part_lse);
         fp.out = outb;
+        fp.out_v8 = aligned(outb, 32) ? 1 : 0;
         fp.lse = lse;
         fp.num_blocks = num_blocks;
         fp.max_blocks = max_blocks_per_req;

@@ -278,6 +278,14 @@ PKA_DEVICE uint32_t pack_bf16(float lo, float hi) {
 PKA_DEVICE float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 PKA_DEVICE float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
+// One 32-byte global store (sm_100 and later); p must be 32-byte aligned.
+PKA_DEVICE void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4, uint32_t a5,
+                             uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 // max(a, b, c) in one instruction (three-input max, sm_100 and later).
 PKA_DEVICE float fmax3f(float a, float b, float c) {
     float d;

@@ -598,30 +598,44 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                                            : (((int64_t)p.ext_base[U.r - p.num_decodes] + (int64_t)U.slot * U.qlen + qi) *
                                                   p.Hq + U.h);
             const float inv = 1.f / l;
+            // 64 columns per TMEM round trip; each thread writes its own row,
+            // 32 bytes (one whole sector) per store where the output allows
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tO + c * 32, r);
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t r[64];
+                tmem_ld32(tO + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+                tmem_ld32(tO + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
                 tmem_wait_ld();
                 if (write) {
                     if (final_out) {
-                        __nv_bfloat16* dst = p.out + orow * D + c * 32;
+                        __nv_bfloat16* dst = p.out + orow * D + c * 64;
+                        uint32_t pk[32];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 v;
-                            v.x = pack_bf16(__uint_as_float(r[j * 8 + 0]) * inv, __uint_as_float(r[j * 8 + 1]) * inv);
-                            v.y = pack_bf16(__uint_as_float(r[j * 8 + 2]) * inv, __uint_as_float(r[j * 8 + 3]) * inv);
-                            v.z = pack_bf16(__uint_as_float(r[j * 8 + 4]) * inv, __uint_as_float(r[j * 8 + 5]) * inv);
-                            v.w = pack_bf16(__uint_as_float(r[j * 8 + 6]) * inv, __uint_as_float(r[j * 8 + 7]) * inv);
-                            *reinterpret_cast<uint4*>(dst + j * 8) = v;
+                        for (int j = 0; j < 32; ++j)
+                            pk[j] = pack_bf16(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
+                        if (p.out_v8) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                st_global_v8(dst + j * 16, pk[8 * j], pk[8 * j + 1], pk[8 * j + 2], pk[8 * j + 3],
+                                             pk[8 * j + 4], pk[8 * j + 5], pk[8 * j + 6], pk[8 * j + 7]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                *reinterpret_cast<uint4*>(dst + j * 8) =
+                                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                         }
                     } else {
-                        float* dst = p.ext_o + orow * D + c * 32;
+                        float* dst = p.ext_o + orow * D + c * 64;  // workspace: 256-byte aligned rows
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<float4*>(dst + j * 4) =
-                                make_float4(__uint_as_float(r[j * 4]) * inv, __uint_as_float(r[j * 4 + 1]) * inv,
-                                            __uint_as_float(r[j * 4 + 2]) * inv, __uint_as_float(r[j * 4 + 3]) * inv);
+                            st_global_v8(dst + j * 8, __float_as_uint(__uint_as_float(r[8 * j]) * inv),
+                                         __float_as_uint(__uint_as_float(r[8 * j + 1]) * inv),
+                                         __float_as_uint(__uint_as_float(r[8 * j + 2]) * inv),
+                                         __float_as_uint(__uint_as_float(r[8 * j + 3]) * inv),
+                                         __float_as_uint(__uint_as_float(r[8 * j + 4]) * inv),
+                                         __float_as_uint(__uint_as_float(r[8 * j + 5]) * inv),
+                                         __float_as_uint(__uint_as_float(r[8 * j + 6]) * inv),
+                                         __float_as_uint(__uint_as_float(r[8 * j + 7]) * inv));
                     }
                 }
             }

@@ -70,6 +70,7 @@ struct FaParams {
     float* lse;
     int64_t num_blocks;
     int max_blocks, Hq, Hkv, G, bs, chunk, num_decodes, num_extends;
+    int out_v8;  // out is 32-byte aligned: rows go out in 32-byte stores
     float scale_log2;
 };
 

@@ -285,3 +285,23 @@ def test_workspace_too_small_is_rejected():
                                    s.scale, s.context_chunk, db.max_query_len, db.max_seq_len, db.out,
                                    db.lse, small)
     assert ei.value.status == 3
+
+
+def test_output_only_16_byte_aligned():
+    """out 16- but not 32-byte aligned: the prefill/extend epilogue falls back
+    from 32-byte to 16-byte stores, with the same results."""
+    import torch
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    spec = W.spec_custom("al16", ctx=[40, 0, 0], qlen=[33, 70, 200], num_decodes=0, num_extends=1,
+                         num_prefills=2, Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=32, seed=16)
+    batch = W.make_batch(spec)
+    db = DeviceBatch(batch)
+    db.cache_write()
+    T, Hq, dv = spec.num_tokens, spec.num_q_heads, spec.head_dim_v
+    buf = torch.zeros(T * Hq * dv + 8, dtype=torch.bfloat16, device=db.device)
+    out = buf[8:].view(T, Hq, dv)
+    assert out.data_ptr() % 32 == 16
+    db.forward(out=out)
+    torch.cuda.synchronize()
+    assert db.error_word() == 0
+    compare(batch, out.float().cpu().numpy().reshape(-1, dv), db.lse.cpu().numpy().reshape(-1))
