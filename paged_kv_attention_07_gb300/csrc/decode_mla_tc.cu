@@ -454,13 +454,15 @@ __global__ void __launch_bounds__(kMtThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kMtTile; ++k) s[k] = k < valid ? s[k] : -INFINITY;
                 }
+                // row max with three-input max (two scores per instruction), 8 chains
                 float mv[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mv[k] = s[k];
+                for (int k = 0; k < 8; ++k) mv[k] = fmaxf(s[k], s[8 + k]);
+                static_assert(kMtTile % 16 == 0, "tile");
 #pragma unroll
-                for (int k = 8; k < kMtTile; k += 8)
+                for (int k = 16; k < kMtTile; k += 16)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) mv[j] = fmaxf(mv[j], s[k + j]);
+                    for (int j = 0; j < 8; ++j) mv[j] = fmax3f(mv[j], s[k + j], s[k + 8 + j]);
                 const float mx = fmaxf(fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])),
                                        fmaxf(fmaxf(mv[4], mv[5]), fmaxf(mv[6], mv[7])));
                 const float m_new = fmaxf(m_used, mx * sl2);
@@ -475,15 +477,17 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                     m_used = m_new;
                 }
                 uint32_t pk[kMtTile / 2];
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int k = 0; k < kMtTile; k += 2) {
-                    const float e0 = fast_exp2(fmaf(s[k], sl2, -m_used));
-                    const float e1 = fast_exp2(fmaf(s[k + 1], sl2, -m_used));
-                    ls[(k >> 1) & 3] += e0 + e1;
+                for (int k = 0; k < kMtTile; k += 2) {  // packed fp32 FMA and add: two scores per instruction
+                    float x0, x1;
+                    fma2_bcast(x0, x1, s[k], s[k + 1], sl2, -m_used);
+                    const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                    const int j = (k >> 1) & 3;
+                    add2(ls[2 * j], ls[2 * j + 1], e0, e1);
                     pk[k / 2] = pack_bf16(e0, e1);
                 }
-                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 // the previous P . V must be done before P or O change
                 if (t > 0) {
                     if (!mbar_wait_warp(pv_done, pv_seen & 1, p.err)) { ok = false; break; }
