@@ -266,6 +266,26 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
         res[name] = ent
         del db
         torch.cuda.empty_cache()
+    # the mixed batch arriving in a shuffled request order: each step gathers
+    # the rows into [decode : extend : prefill] order and the outputs back
+    # (pka_batch_order + pka_gather_rows); roofline of the gather kernel
+    import numpy as np
+    from paged_kv_attention_07_gb300.device_batch import UnorderedBatch
+    spec = W.spec_mixed()
+    db = make_device_batch(spec, device, seed=1234 + rank)
+    ub = UnorderedBatch(db, np.random.default_rng(5).permutation(spec.num_reqs))
+    ms, stats, launches, _ = time_steps(ub, steps, warmup)
+    ent = {"ms_per_step": round(ms, 4), "kernels": {k: round(v["avg_ms"], 4) for k, v in stats.items()},
+           "gather_bytes_per_step": ub.gather_bytes}
+    gk = stats.get("gather")
+    if gk:
+        gather_ms = gk["avg_ms"] * gk["launches"] / steps  # the step's 8 gathers together
+        ent["gather_ms_per_step"] = round(gather_ms, 4)
+        ent["roofline"] = roofline("hbm", ub.gather_bytes / (gather_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                                   None)
+    res["mixed_unordered"] = ent
+    del ub, db
+    torch.cuda.empty_cache()
     return res
 
 

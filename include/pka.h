@@ -77,6 +77,7 @@ typedef enum {
 #define PKA_DEVERR_SLOT 0x40            /* a cache slot >= num_blocks * block_size */
 #define PKA_DEVERR_CAPACITY 0x80        /* the plan outgrew the workspace (inconsistent hints) */
 #define PKA_DEVERR_TIMEOUT 0x100        /* a pipeline wait gave up (bounded spin); results invalid */
+#define PKA_DEVERR_INDEX 0x200          /* pka_gather_rows: a row index outside [0, src_rows) */
 
 /*
  * pka_cache_write -- write the new tokens' K and V rows into the paged cache.
@@ -265,13 +266,54 @@ typedef enum {
     PKA_KERNEL_PREFILL_EXTEND = 4,  /* varlen prefill + extend stages */
     PKA_KERNEL_EXTEND_REDUCE = 5,
     PKA_KERNEL_MERGE = 6,
-    PKA_KERNEL_COUNT = 7
+    PKA_KERNEL_GATHER = 7,          /* pka_gather_rows */
+    PKA_KERNEL_COUNT = 8
 } pka_kernel;
 
 /* enable != 0 turns timing on for `kernel` (and resets it); 0 turns it off. */
 PKA_API pka_status pka_kernel_timer(int kernel, int enable);
 /* Summed duration (ms) and launch count of `kernel` since it was enabled. */
 PKA_API pka_status pka_kernel_timer_read(int kernel, double *total_ms, int *launches, int *timed);
+
+/*
+ * pka_batch_order -- put a batch of requests in the order the forward pass
+ * needs, [decode : extend : prefill] (the pages' batch reordering before the
+ * attention backend; classification with the decode threshold 1: a request
+ * with one new token is a decode, one with more new tokens and cached context
+ * an extend, one without cached context a prefill). Host-only, no CUDA call.
+ *
+ *   num_reqs      B >= 1
+ *   query_lens    [B] new tokens per request, >= 1 (host)
+ *   ctx_lens      [B] cached tokens per request before this step, >= 0 (host)
+ *   req_order     [B] out: req_order[i] = original index of the request at
+ *                 position i; stable within each class
+ *   qsl_ordered   [B+1] out: query_start_loc of the ordered batch
+ *   token_src     [T] out (T = sum of query_lens; may be NULL): original
+ *                 token row of ordered token row j (gather index for q, k, v)
+ *   token_dst     [T] out (may be NULL): ordered token row of original token
+ *                 row t (gather index that brings out/lse back)
+ *   counts        [3] out: num_decodes, num_extends, num_prefills
+ * Returns PKA_ERR_INVALID_ARG for B < 1, a NULL required pointer, a query
+ * length < 1 or a context length < 0 (outputs untouched), else PKA_OK.
+ */
+PKA_API pka_status pka_batch_order(int num_reqs, const int32_t *query_lens, const int32_t *ctx_lens,
+                                   int32_t *req_order, int32_t *qsl_ordered, int32_t *token_src,
+                                   int32_t *token_dst, int32_t *counts);
+
+/*
+ * pka_gather_rows -- dst row i = src row index[i], for i in [0, num_rows):
+ * moves token rows (q, k, v, out, lse) or request rows (seq_lens, block
+ * table rows) into or out of the order of pka_batch_order. Device pointers;
+ * rows are row_bytes long and packed (row i at byte offset i * row_bytes).
+ * 16-byte copies when row_bytes and both pointers allow, else 4-byte, else
+ * single bytes. A row whose index is outside [0, src_rows) is zero-filled
+ * and, when error_word is given, PKA_DEVERR_INDEX is OR-ed into it. dst and
+ * src must not overlap. Asynchronous on `stream`.
+ * Returns PKA_ERR_INVALID_ARG for NULL dst/src/index, num_rows < 0,
+ * src_rows < 0 or row_bytes < 1, PKA_ERR_CUDA on a launch failure.
+ */
+PKA_API pka_status pka_gather_rows(void *dst, const void *src, const int32_t *index, int64_t num_rows,
+                                   int64_t src_rows, int64_t row_bytes, int32_t *error_word, void *stream);
 
 /*
  * pka_selftest_wait -- the library's bounded pipeline wait (the one every

@@ -27,6 +27,8 @@ cudaError_t launch_decode_mla(const CUtensorMap& map, const DecodeMlaParams& p, 
                               cudaStream_t stream);
 cudaError_t launch_fa_fwd(const FaMaps& maps, const FaParams& p, int head_dim, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode_reduce(const DecodeReduceParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t num_rows, int64_t src_rows,
+                               int64_t row_bytes, int32_t* err, int num_sms, cudaStream_t stream);
 cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bound, int num_sms,
                                  cudaStream_t stream);
 int decode_gqa_target_units(int num_sms);
@@ -590,6 +592,18 @@ pka_status pka_merge_attn_states(void* out, float* out_lse, const void* prefix_o
     return cuda_status(timed(PKA_KERNEL_MERGE, st, [&] {
         return launch_merge_pair(out, out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse, num_rows, head_dim,
                                  io_dtype, sms, st);
+    }));
+}
+
+pka_status pka_gather_rows(void* dst, const void* src, const int32_t* index, int64_t num_rows, int64_t src_rows,
+                           int64_t row_bytes, int32_t* error_word, void* stream) {
+    if (!dst || !src || !index || num_rows < 0 || src_rows < 0 || row_bytes < 1) return PKA_ERR_INVALID_ARG;
+    if (error_word && !aligned(error_word, 4)) return PKA_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return PKA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(timed(PKA_KERNEL_GATHER, st, [&] {
+        return launch_gather_rows(dst, src, index, num_rows, src_rows, row_bytes, error_word, sms, st);
     }));
 }
 

@@ -89,3 +89,62 @@ class DeviceBatch:
 
     def error_word(self) -> int:
         return pka.pka_get_error(self.workspace)
+
+
+class UnorderedBatch:
+    """A DeviceBatch whose requests arrive in another order: user request i is
+    batch request perm[i]. A step does what a server does with such a batch:
+    the token and request rows are gathered into [decode : extend : prefill]
+    order (pka_batch_order's maps, computed once on the host from the
+    lengths), cache write and forward run on the ordered rows, and out / lse
+    are gathered back into the user's order (out_u, lse_u)."""
+
+    def __init__(self, db: DeviceBatch, perm):
+        b, dev = db.batch, db.device
+        qsl0 = np.asarray(b.query_start_loc, dtype=np.int64)
+        qlen = np.diff(qsl0).astype(np.int32)
+        ctx = (np.asarray(b.seq_lens, dtype=np.int64) - qlen).astype(np.int32)
+        perm = np.asarray(perm, dtype=np.int64)
+        self.tok_u = np.concatenate([np.arange(qsl0[r], qsl0[r + 1]) for r in perm])
+        idx = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+        sel = lambda t, a: None if t is None else t.index_select(0, idx(a).long()).contiguous()
+        self.db = db
+        # the rows as the user hands them over (set up once, outside the step)
+        self.q_u, self.k_u, self.v_u = sel(db.q, self.tok_u), sel(db.k_new, self.tok_u), sel(db.v_new, self.tok_u)
+        self.slot_u = sel(db.slot_mapping, self.tok_u)
+        self.seq_u, self.bt_u = sel(db.seq_lens, perm), sel(db.block_table, perm)
+        order, qsl_o, src, dst, counts = pka.pka_batch_order(qlen[perm], ctx[perm])
+        self.counts = [int(c) for c in counts]
+        self.src, self.dst, self.order, self.qsl_o = idx(src), idx(dst), idx(order), idx(qsl_o)
+        empty = lambda t: None if t is None else torch.empty_like(t)
+        self.q_o, self.k_o, self.v_o, self.slot_o = empty(self.q_u), empty(self.k_u), empty(self.v_u), empty(self.slot_u)
+        self.seq_o, self.bt_o = empty(self.seq_u), empty(self.bt_u)
+        self.out_o, self.lse_o = torch.empty_like(db.out), torch.empty_like(db.lse)
+        self.out_u, self.lse_u = torch.empty_like(db.out), torch.empty_like(db.lse)
+        rows = lambda t: 0 if t is None else t.numel() * t.element_size()
+        # bytes the gathers read and write per step
+        self.gather_bytes = 2 * sum(rows(t) for t in (self.q_u, self.k_u, self.v_u, self.slot_u, self.seq_u,
+                                                       self.bt_u, self.out_o, self.lse_o))
+        torch.cuda.synchronize()
+
+    def step(self, stream=None):
+        g = pka.pka_gather_rows
+        col = lambda t: t.view(-1, 1)
+        g(self.q_o, self.q_u, self.src, stream=stream)
+        g(self.k_o, self.k_u, self.src, stream=stream)
+        if self.v_u is not None:
+            g(self.v_o, self.v_u, self.src, stream=stream)
+        g(col(self.slot_o), col(self.slot_u), self.src, stream=stream)
+        g(col(self.seq_o), col(self.seq_u), self.order, stream=stream)
+        g(self.bt_o, self.bt_u, self.order, stream=stream)
+        db, s = self.db, self.db.spec
+        pka.pka_cache_write(self.k_o, self.v_o, self.slot_o, db.k_cache, db.v_cache, stream=stream)
+        pka.pka_paged_attn_forward(self.q_o, self.k_o, self.v_o, db.k_cache, db.v_cache, self.bt_o, self.qsl_o,
+                                   self.seq_o, self.counts[0], self.counts[1], self.counts[2], s.scale,
+                                   s.context_chunk, db.max_query_len, db.max_seq_len, self.out_o, self.lse_o,
+                                   db.workspace, head_dim_v=s.head_dim_v, stream=stream)
+        g(self.out_u, self.out_o, self.dst, stream=stream)
+        g(self.lse_u, self.lse_o, self.dst, stream=stream)
+
+    def error_word(self) -> int:
+        return self.db.error_word()

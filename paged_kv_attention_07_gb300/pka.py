@@ -17,12 +17,14 @@ PKA_OK = 0
 STATUS_NAMES = {0: "PKA_OK", 1: "PKA_ERR_INVALID_ARG", 2: "PKA_ERR_UNSUPPORTED",
                 3: "PKA_ERR_WORKSPACE_TOO_SMALL", 4: "PKA_ERR_CUDA", 5: "PKA_ERR_DEVICE_METADATA"}
 DEVERR = {"QUERY_START_LOC": 0x01, "SEQ_LEN": 0x02, "ORDER": 0x04, "QUERY_LEN": 0x08,
-          "BLOCK_TABLE": 0x10, "BLOCK_ID": 0x20, "SLOT": 0x40, "CAPACITY": 0x80, "TIMEOUT": 0x100}
+          "BLOCK_TABLE": 0x10, "BLOCK_ID": 0x20, "SLOT": 0x40, "CAPACITY": 0x80, "TIMEOUT": 0x100,
+          "INDEX": 0x200}
 EXPORTED = ("pka_cache_write", "pka_workspace_size", "pka_paged_attn_forward",
             "pka_merge_attn_states", "pka_get_error", "pka_paged_decode_noalloc", "pka_kernel_timer",
-            "pka_kernel_timer_read", "pka_selftest_wait", "pka_status_string")
+            "pka_kernel_timer_read", "pka_batch_order", "pka_gather_rows", "pka_selftest_wait",
+            "pka_status_string")
 KERNELS = {"cache_write": 0, "planner": 1, "decode": 2, "decode_reduce": 3, "prefill_extend": 4,
-           "extend_reduce": 5, "merge": 6}
+           "extend_reduce": 5, "merge": 6, "gather": 7}
 
 
 class PkaError(RuntimeError):
@@ -69,6 +71,10 @@ def load(path: str | None = None):
     lib.pka_kernel_timer_read.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                                           ctypes.POINTER(ctypes.c_int)]
     lib.pka_status_string.restype = ctypes.c_char_p
+    lib.pka_batch_order.restype = i32
+    lib.pka_batch_order.argtypes = [i32, P, P, P, P, P, P, P]
+    lib.pka_gather_rows.restype = i32
+    lib.pka_gather_rows.argtypes = [P, P, P, i64, i64, i64, P, P]
     lib.pka_selftest_wait.argtypes = [i32, ctypes.c_uint32, ctypes.POINTER(ctypes.c_int32), P]
     lib.pka_selftest_wait.restype = i32
     lib.pka_status_string.argtypes = [i32]
@@ -164,6 +170,34 @@ def pka_kernel_timer_read(kernel: str):
     _check(load().pka_kernel_timer_read(KERNELS[kernel], ctypes.byref(ms), ctypes.byref(n),
                                         ctypes.byref(t)), "pka_kernel_timer_read")
     return float(ms.value), int(n.value), int(t.value)
+
+
+def pka_batch_order(query_lens, ctx_lens):
+    """Order a batch as [decode : extend : prefill] (host arrays, see include/pka.h).
+    Returns (req_order[B], qsl_ordered[B+1], token_src[T], token_dst[T], counts[3]) as
+    int32 numpy arrays."""
+    import numpy as np
+    q = np.ascontiguousarray(query_lens, dtype=np.int32)
+    c = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    B, T = int(q.shape[0]), int(q.sum()) if q.size else 0
+    order = np.zeros(B, np.int32)
+    qsl = np.zeros(B + 1, np.int32)
+    src = np.zeros(max(T, 1), np.int32)
+    dst = np.zeros(max(T, 1), np.int32)
+    counts = np.zeros(3, np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(load().pka_batch_order(B, p(q), p(c), p(order), p(qsl), p(src), p(dst), p(counts)), "pka_batch_order")
+    return order, qsl, src[:T], dst[:T], counts
+
+
+def pka_gather_rows(dst, src, index, error_word=None, stream=None):
+    """dst[i] = src[index[i]] over the first dimension (packed rows); index is a
+    CUDA int32 tensor of len(dst) entries."""
+    if dst.shape[0] == 0:
+        return
+    row_bytes = dst[0].numel() * dst.element_size()
+    _check(load().pka_gather_rows(_ptr(dst), _ptr(src), _ptr(index), int(dst.shape[0]), int(src.shape[0]),
+                                  int(row_bytes), _ptr(error_word), _stream(stream)), "pka_gather_rows")
 
 
 def pka_selftest_wait(arrive: bool, limit_us: int, stream=None) -> int:

@@ -1,0 +1,84 @@
+"""A batch that arrives in any request order: pka_batch_order orders it as
+[decode : extend : prefill], pka_gather_rows moves the token and request rows
+into that order and the outputs back, and the result matches the oracle of the
+same requests. Also: the whole step replays from a CUDA graph bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_07_gb300 import pka
+from paged_kv_attention_07_gb300 import workloads as W
+from paged_kv_attention_07_gb300.device_batch import DeviceBatch, UnorderedBatch
+from tests.gpu_util import LSE_ATOL, OUT_ATOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_shuffled_batch_through_order_and_gather(seed):
+    # the workload builder makes an ordered batch; the user's batch is a shuffle of it
+    spec = W.spec_custom("ordered", ctx=[3, 700, 77, 40, 1500, 0, 0], qlen=[1, 1, 1, 33, 70, 100, 7],
+                         num_decodes=3, num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=128, dv=128, bs=16,
+                         chunk=512, seed=40 + seed)
+    batch = W.make_batch(spec)
+    db = DeviceBatch(batch)
+    perm = np.random.default_rng(seed).permutation(spec.num_reqs)
+    ub = UnorderedBatch(db, perm)
+    assert ub.counts == [3, 2, 2]
+    ub.step()
+    torch.cuda.synchronize()
+    assert ub.error_word() == 0
+    ref_o, ref_l = oracle.batch_reference(batch)
+    Hq, dv = spec.num_q_heads, spec.head_dim_v
+    rows = (ub.tok_u[:, None] * Hq + np.arange(Hq)[None, :]).reshape(-1)
+    eo = np.abs(ub.out_u.float().cpu().numpy().reshape(-1, dv) - ref_o[rows]).max()
+    el = np.abs(ub.lse_u.cpu().numpy().reshape(-1) - ref_l[rows]).max()
+    assert eo <= OUT_ATOL and el <= LSE_ATOL, (eo, el)
+
+
+def test_gather_rows_bad_index_zero_fills_and_flags():
+    src = torch.arange(40, dtype=torch.float32, device="cuda").view(10, 4)
+    idx = torch.tensor([3, -1, 9, 10], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dst = torch.full((4, 4), 7.0, device="cuda")
+    pka.pka_gather_rows(dst, src, idx, error_word=err)
+    torch.cuda.synchronize()
+    assert torch.equal(dst[0], src[3]) and torch.equal(dst[2], src[9])
+    assert torch.all(dst[1] == 0) and torch.all(dst[3] == 0)
+    assert int(err.item()) == pka.DEVERR["INDEX"]
+
+
+@pytest.mark.parametrize("row_bytes", [1, 6, 12, 16, 8192])
+def test_gather_rows_widths(row_bytes):
+    g = torch.Generator(device="cuda").manual_seed(row_bytes)
+    src = torch.randint(0, 255, (33, row_bytes), dtype=torch.uint8, device="cuda", generator=g)
+    idx = torch.randint(0, 33, (50,), dtype=torch.int32, device="cuda", generator=g)
+    dst = torch.empty((50, row_bytes), dtype=torch.uint8, device="cuda")
+    pka.pka_gather_rows(dst, src, idx)
+    torch.cuda.synchronize()
+    assert torch.equal(dst, src[idx.long()])
+
+
+def test_step_replays_from_a_cuda_graph():
+    spec = W.spec_custom("graph", ctx=[3, 700, 40, 1500, 0, 0], qlen=[1, 1, 33, 70, 100, 7], num_decodes=2,
+                         num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=128, dv=128, bs=16, chunk=512, seed=7)
+    db = DeviceBatch(W.make_batch(spec))
+    db.step()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = db.out.clone(), db.lse.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        db.step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        db.step()
+    db.out.zero_()
+    db.lse.zero_()
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert db.error_word() == 0
+    assert torch.equal(db.out, ref_out) and torch.equal(db.lse, ref_lse)
