@@ -3,6 +3,7 @@
 // "Key innovations", batch reordering; the decode threshold is 1 new token)
 // and a device row gather that moves token and request rows into and out of
 // that order.
+#include <algorithm>
 #include <vector>
 
 #include "common.cuh"
@@ -10,13 +11,15 @@
 namespace pka {
 
 // dst row i = src row idx[i]; V = 16, 4 or 1 bytes per copy, rows of
-// `vecs` copies. A grid-stride loop over (row, copy) pairs.
-template <typename V>
+// `vecs` copies: a grid-stride loop over (row, copy) pairs, consecutive
+// threads on consecutive copies of a row (coalesced). I is the index type of
+// that loop: 32-bit while the total fits (a cheaper division), else 64-bit.
+template <typename V, typename I>
 __global__ void gather_rows_kernel(V* __restrict__ dst, const V* __restrict__ src, const int32_t* __restrict__ idx,
-                                   int64_t num_rows, int64_t src_rows, int64_t vecs, int32_t* err) {
-    const int64_t total = num_rows * vecs;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = e / vecs, c = e - row * vecs;
+                                   I num_rows, int64_t src_rows, I vecs, int32_t* err) {
+    const I total = num_rows * vecs;
+    for (I e = (I)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (I)gridDim.x * blockDim.x) {
+        const I row = e / vecs, c = e - row * vecs;
         const int32_t s = __ldg(idx + row);
         if (s < 0 || s >= src_rows) {
             dst[e] = V{};
@@ -43,10 +46,15 @@ cudaError_t launch_gather_rows(void* dst, const void* src, const int32_t* idx, i
         const int64_t vecs = row_bytes / bytes;
         const int64_t total = num_rows * vecs;
         const int threads = 256;
-        const int64_t want = (total + threads - 1) / threads;
-        const int blocks = (int)std::min<int64_t>(want, (int64_t)num_sms * 8);
-        gather_rows_kernel<V><<<blocks, threads, 0, stream>>>(static_cast<V*>(dst), static_cast<const V*>(src), idx,
-                                                               num_rows, src_rows, vecs, err);
+        const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads,
+                                                                       (int64_t)num_sms * 8));
+        if (total < ((int64_t)1 << 31))
+            gather_rows_kernel<V, uint32_t><<<blocks, threads, 0, stream>>>(
+                static_cast<V*>(dst), static_cast<const V*>(src), idx, (uint32_t)num_rows, src_rows,
+                (uint32_t)vecs, err);
+        else
+            gather_rows_kernel<V, int64_t><<<blocks, threads, 0, stream>>>(
+                static_cast<V*>(dst), static_cast<const V*>(src), idx, num_rows, src_rows, vecs, err);
         return cudaGetLastError();
     };
     if (row_bytes % 16 == 0 && (a & 15) == 0) return go(V16{}, 16);

@@ -37,11 +37,12 @@ def test_shuffled_batch_through_order_and_gather(seed):
     assert eo <= OUT_ATOL and el <= LSE_ATOL, (eo, el)
 
 
-def test_gather_rows_bad_index_zero_fills_and_flags():
-    src = torch.arange(40, dtype=torch.float32, device="cuda").view(10, 4)
+@pytest.mark.parametrize("width", [4, 1024])  # 16-byte rows (flat loop), 4 KB rows (a warp per row)
+def test_gather_rows_bad_index_zero_fills_and_flags(width):
+    src = torch.arange(10 * width, dtype=torch.float32, device="cuda").view(10, width)
     idx = torch.tensor([3, -1, 9, 10], dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    dst = torch.full((4, 4), 7.0, device="cuda")
+    dst = torch.full((4, width), 7.0, device="cuda")
     pka.pka_gather_rows(dst, src, idx, error_word=err)
     torch.cuda.synchronize()
     assert torch.equal(dst[0], src[3]) and torch.equal(dst[2], src[9])
