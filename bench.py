@@ -147,10 +147,10 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm
-def make_device_batch(spec, device, seed):
+def make_device_batch(spec, device, seed, unified=False):
     from paged_kv_attention_07_gb300.device_batch import DeviceBatch
     batch = W.make_batch(spec, values=False)
-    return DeviceBatch(batch, device=device, values_on_device_seed=seed)
+    return DeviceBatch(batch, device=device, values_on_device_seed=seed, unified=unified)
 
 
 def time_steps(db, steps, warmup, flush_bytes=0, kernels=(), barrier=None):
@@ -266,6 +266,23 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
         res[name] = ent
         del db
         torch.cuda.empty_cache()
+    # single-path routing of the same mixed batch: the decodes go through the
+    # prefill/extend kernel as one-token extends (num_decodes 0); compared with
+    # the three-path step above
+    spec = W.spec_mixed()
+    db = make_device_batch(spec, device, seed=1234 + rank, unified=True)
+    ms, stats, launches, _ = time_steps(db, steps, warmup)
+    w = algorithmic_work(spec)
+    ent = {"ms_per_step": round(ms, 4), "tokens_per_s": round(w["tokens"] / (ms * 1e-3), 1),
+           "kernels": {k: round(v["avg_ms"], 4) for k, v in stats.items()},
+           "three_path_ms_per_step": res.get("mixed", {}).get("ms_per_step")}
+    kms = stats.get("prefill_extend", {}).get("avg_ms")
+    if kms:
+        flops = w["dec_flops"] + w["ext_flops"] + w["pre_flops"]
+        ent["roofline"] = roofline("tensor", flops / (kms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s", None)
+    res["mixed_unified"] = ent
+    del db
+    torch.cuda.empty_cache()
     # the mixed batch arriving in a shuffled request order: each step gathers
     # the rows into [decode : extend : prefill] order and the outputs back
     # (pka_batch_order + pka_gather_rows); roofline of the gather kernel

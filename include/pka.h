@@ -130,7 +130,10 @@ PKA_API size_t pka_workspace_size(int num_decodes, int num_extends, int num_pref
  *
  * Batch layout (the model runner's reorder, "Key innovations" item 2): the
  * first num_decodes requests are decodes (query_len == 1), the next
- * num_extends are extends (query_len >= 2 and ctx >= 1), the last
+ * num_extends are extends (ctx >= 1; query_len >= 2 normally, but a request
+ * with one new token may be placed here too: it then runs through the
+ * extend path instead of the decode kernel, which is how a caller gets the
+ * single-path "unified" routing of every request with context), the last
  * num_prefills are prefills (ctx == 0). New tokens are contiguous per
  * request: request r owns rows [query_start_loc[r], query_start_loc[r+1]).
  *

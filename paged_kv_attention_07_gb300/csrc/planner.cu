@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
             if (ql != 1) err |= PKA_DEVERR_ORDER;
             dec_keys += (unsigned long long)(s > 0 ? s : 0);
         } else if (r < nd + ne) {
-            if (ql < 2 || ctx < 1) err |= PKA_DEVERR_ORDER;
+            if (ctx < 1) err |= PKA_DEVERR_ORDER;  // one new token here takes the extend path
         } else if (ctx != 0) {
             err |= PKA_DEVERR_ORDER;
         }

@@ -20,9 +20,14 @@ def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
 
 
 class DeviceBatch:
-    def __init__(self, batch: W.Batch, device="cuda", values_on_device_seed: int | None = None):
+    def __init__(self, batch: W.Batch, device="cuda", values_on_device_seed: int | None = None,
+                 unified: bool = False):
         spec = batch.spec
         self.batch, self.spec, self.device = batch, spec, device
+        # unified: the decodes go in the extend slice (num_decodes 0), so every
+        # request with context runs through the extend path
+        nd = 0 if unified else spec.num_decodes
+        self.counts = (nd, spec.num_extends + spec.num_decodes - nd, spec.num_prefills)
         Hq, Hkv, d, dv, bs = (spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.head_dim_v,
                               spec.block_size)
         T = spec.num_tokens
@@ -62,8 +67,8 @@ class DeviceBatch:
         self.lse = torch.zeros((T, Hq), dtype=torch.float32, device=device)
         self.max_query_len = int(max(spec.qlen))
         self.max_seq_len = int(max(spec.seq_lens))
-        ws = pka.pka_workspace_size(spec.num_decodes, spec.num_extends, spec.num_prefills, T, Hq, Hkv,
-                                    d, dv, self.max_query_len, self.max_seq_len, spec.context_chunk)
+        ws = pka.pka_workspace_size(*self.counts, T, Hq, Hkv, d, dv, self.max_query_len, self.max_seq_len,
+                                    spec.context_chunk)
         if ws == 0:
             raise RuntimeError("pka_workspace_size rejected the batch shape")
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
@@ -76,8 +81,8 @@ class DeviceBatch:
     def forward(self, stream=None, out=None, lse=None):
         s = self.spec
         pka.pka_paged_attn_forward(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
-                                   self.block_table, self.qsl, self.seq_lens, s.num_decodes,
-                                   s.num_extends, s.num_prefills, s.scale, s.context_chunk,
+                                   self.block_table, self.qsl, self.seq_lens, *self.counts, s.scale,
+                                   s.context_chunk,
                                    self.max_query_len, self.max_seq_len,
                                    self.out if out is None else out,
                                    self.lse if lse is None else lse, self.workspace,

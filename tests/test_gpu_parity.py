@@ -235,6 +235,7 @@ def test_device_error_order():
     db = _with_metadata(W.make_batch(spec))
     db.spec = W.spec_custom("ord", ctx=[10, 0], qlen=[1, 5], num_decodes=2, num_extends=0,
                             num_prefills=0, Hq=4, Hkv=2, d=64, dv=64, bs=16)
+    db.counts = (2, 0, 0)
     db.workspace = torch.zeros(db.workspace.numel() + (4 << 20), dtype=torch.uint8, device="cuda")
     db.out.fill_(7.0)
     db.forward()
@@ -305,3 +306,21 @@ def test_output_only_16_byte_aligned():
     torch.cuda.synchronize()
     assert db.error_word() == 0
     compare(batch, out.float().cpu().numpy().reshape(-1, dv), db.lse.cpu().numpy().reshape(-1))
+
+
+@pytest.mark.parametrize("bs", [1, 16])
+def test_decodes_routed_through_the_extend_path(bs):
+    """The single-path routing: decodes placed in the extend slice (num_decodes
+    0) run through the prefill/extend kernel and its chunk merge, same results."""
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    spec = W.spec_custom("unified", ctx=[3, 700, 1, 40, 2000, 0, 0], qlen=[1, 1, 1, 33, 70, 100, 7],
+                         num_decodes=3, num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=128, dv=128, bs=bs,
+                         chunk=512, seed=11 + bs)
+    batch = W.make_batch(spec)
+    db = DeviceBatch(batch, unified=True)
+    assert db.counts == (0, 5, 2)
+    db.step()
+    import torch
+    torch.cuda.synchronize()
+    assert db.error_word() == 0
+    compare(batch, db.out.float().cpu().numpy().reshape(-1, spec.head_dim_v), db.lse.cpu().numpy().reshape(-1))
