@@ -435,13 +435,18 @@ def run_ours(args):
 
 WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "prefill_varlen": W.spec_prefill, "mixed": W.spec_mixed,
              "mla_decode_bs64": W.spec_mla_decode,
-             "mla_decode_bs1": lambda: W.spec_mla_decode(block_size=1)}
+             "mla_decode_bs1": lambda: W.spec_mla_decode(block_size=1),
+             "mixed_unified": W.spec_mixed, "mixed_unordered": W.spec_mixed}
 
 
 def profile_workload(args, device):
     """Run --steps steps of one workload and print its timing (for profilers)."""
     spec = WORKLOADS[args.workload]()
-    db = make_device_batch(spec, device, seed=7)
+    db = make_device_batch(spec, device, seed=7, unified=args.workload == "mixed_unified")
+    if args.workload == "mixed_unordered":
+        import numpy as np
+        from paged_kv_attention_07_gb300.device_batch import UnorderedBatch
+        db = UnorderedBatch(db, np.random.default_rng(5).permutation(spec.num_reqs))
     ms, stats, launches, _ = time_steps(db, args.steps, args.warmup)
     print(json.dumps({"workload": args.workload, "ms_per_step": ms,
                       "kernels_ms": {k: v["avg_ms"] for k, v in stats.items()}, "gpu_launches": launches}))
