@@ -313,7 +313,8 @@ PKA_API pka_status pka_batch_order(int num_reqs, const int32_t *query_lens, cons
  * and, when error_word is given, PKA_DEVERR_INDEX is OR-ed into it. dst and
  * src must not overlap. Asynchronous on `stream`.
  * Returns PKA_ERR_INVALID_ARG for NULL dst/src/index, num_rows < 0,
- * src_rows < 0 or row_bytes < 1, PKA_ERR_CUDA on a launch failure.
+ * src_rows < 0, row_bytes < 1 or a byte size past INT64_MAX, PKA_ERR_CUDA
+ * on a launch failure.
  */
 PKA_API pka_status pka_gather_rows(void *dst, const void *src, const int32_t *index, int64_t num_rows,
                                    int64_t src_rows, int64_t row_bytes, int32_t *error_word, void *stream);

@@ -598,6 +598,7 @@ pka_status pka_merge_attn_states(void* out, float* out_lse, const void* prefix_o
 pka_status pka_gather_rows(void* dst, const void* src, const int32_t* index, int64_t num_rows, int64_t src_rows,
                            int64_t row_bytes, int32_t* error_word, void* stream) {
     if (!dst || !src || !index || num_rows < 0 || src_rows < 0 || row_bytes < 1) return PKA_ERR_INVALID_ARG;
+    if (num_rows > INT64_MAX / row_bytes || src_rows > INT64_MAX / row_bytes) return PKA_ERR_INVALID_ARG;
     if (error_word && !aligned(error_word, 4)) return PKA_ERR_INVALID_ARG;
     const int sms = device_sm_count();
     if (sms <= 0) return PKA_ERR_CUDA;

@@ -195,6 +195,12 @@ def pka_gather_rows(dst, src, index, error_word=None, stream=None):
     CUDA int32 tensor of len(dst) entries."""
     if dst.shape[0] == 0:
         return
+    if not (dst.is_contiguous() and src.is_contiguous() and index.is_contiguous()):
+        raise ValueError("pka_gather_rows: dst, src and index must be contiguous (packed rows)")
+    if dst.dtype != src.dtype or dst[0].numel() != src[0].numel() or index.dtype.itemsize != 4:
+        raise ValueError("pka_gather_rows: dst and src rows must match; index must be int32")
+    if index.numel() < dst.shape[0]:
+        raise ValueError("pka_gather_rows: index shorter than dst")
     row_bytes = dst[0].numel() * dst.element_size()
     _check(load().pka_gather_rows(_ptr(dst), _ptr(src), _ptr(index), int(dst.shape[0]), int(src.shape[0]),
                                   int(row_bytes), _ptr(error_word), _stream(stream)), "pka_gather_rows")

@@ -73,3 +73,4 @@ def test_gather_rows_rejects_bad_arguments(lib):
     assert lib.pka_gather_rows(None, buf, buf, 1, 1, 4, None, None) == 1
     assert lib.pka_gather_rows(buf, buf, buf, -1, 1, 4, None, None) == 1
     assert lib.pka_gather_rows(buf, buf, buf, 1, 1, 0, None, None) == 1
+    assert lib.pka_gather_rows(buf, buf, buf, 1 << 62, 1, 16, None, None) == 1  # byte size overflows
