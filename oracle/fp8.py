@@ -1,0 +1,55 @@
+"""FP8 E4M3 codes for a KV cache stored in 8 bits with a per-tensor scale
+(TEST INFRASTRUCTURE, like the rest of `oracle/`; next row f3 of the build:
+the cache the pages' `gather_and_maybe_dequant_cache` step dequantises).
+
+Written from the format's definition (the "fn" variant: no infinities):
+bit 7 sign, bits 6..3 exponent with bias 7, bits 2..0 mantissa. Exponent
+field 0 holds the subnormals m * 2^-9; otherwise the value is
+(1 + m/8) * 2^(e - 7). The all-ones pattern S.1111.111 is NaN, so the largest
+finite magnitude is 1.75 * 2^8 = 448. Encoding rounds to the nearest code,
+ties to the even code, and saturates finite values beyond 448 to +-448.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+MAX_FINITE = 448.0
+
+
+def decode(codes) -> np.ndarray:
+    """float64 value of each 8-bit code (NaN for the two NaN codes)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    out = sign * mag
+    return np.where((c & 0x7F) == 0x7F, np.nan, out)
+
+
+_POS = decode(np.arange(0x7F))  # the 127 non-negative finite values, ascending with the code
+
+
+def encode(x) -> np.ndarray:
+    """Nearest code (ties to the even code), finite values beyond 448
+    saturated to +-448, NaN to 0x7F; the sign of zero is kept."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), MAX_FINITE)
+    hi = np.clip(np.searchsorted(_POS, a, side="left"), 0, len(_POS) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - _POS[lo], _POS[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.int64)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def quantize(x, scale: float) -> np.ndarray:
+    """Codes of x / scale (scale > 0)."""
+    return encode(np.asarray(x, dtype=np.float64) / scale)
+
+
+def dequantize(codes, scale: float) -> np.ndarray:
+    """code value * scale, float64."""
+    return decode(codes) * scale
