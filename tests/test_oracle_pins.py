@@ -68,6 +68,10 @@ SMALL_SPECS = [
                   num_prefills=0, Hq=3, Hkv=3, d=16, dv=16, bs=64, seed=6),
     W.spec_custom("mla_like", ctx=[17, 40], qlen=[1, 1], num_decodes=2, num_extends=0,
                   num_prefills=0, Hq=8, Hkv=1, d=48, dv=32, bs=4, mla=True, seed=7),
+    # separate K and V caches with d != dv: the shape of the non-absorbed MLA
+    # prefill/extend (192 / 128) scaled down (next row f2)
+    W.spec_custom("mha_d24_dv16", ctx=[9, 33, 0], qlen=[1, 12, 5], num_decodes=1, num_extends=1,
+                  num_prefills=1, Hq=4, Hkv=2, d=24, dv=16, bs=8, seed=8),
 ]
 
 
