@@ -24,9 +24,11 @@
 //            keys 0..63 first when the softmax signals that half early;
 //   warps 4-7, 8-11: softmax warpgroup k owns query tile k, one thread per
 //            query row (= TMEM lane), with its own S_k, running max and sum
-//            and O_k. Each reads its S row twice (row max, then exponentials:
-//            the row never sits in registers whole), writes P as bf16 pairs
-//            over the S_k columns it has already consumed, rescales O_k only
+//            and O_k. It reads its S row in 64-column halves: once when the
+//            tile needs no mask and its scores stay within the rescale margin
+//            of the running max, else twice (row max, then exponentials; the
+//            row never sits in registers whole); writes P as bf16 pairs over
+//            the S_k columns it has already consumed, rescales O_k only
 //            when its max grew by more than 2^8 (otherwise the stale max is
 //            kept: P stays <= 2^8; warp-uniform, tcgen05.ld/st being
 //            warp-collective), and ends the unit on its own: O_k / l to out
