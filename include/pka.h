@@ -328,7 +328,8 @@ PKA_API pka_status pka_gather_rows(void *dst, const void *src, const int32_t *in
  * microseconds, records PKA_DEVERR_TIMEOUT in the run's device error word and
  * the kernel exits normally (the CUDA context stays usable). The run's error
  * word (0 or PKA_DEVERR_TIMEOUT) is written to *code_out. Synchronises
- * `stream` (NULL = legacy default stream).
+ * `stream` (NULL = legacy default stream). The run's error word is one
+ * device-global int per process: calls must not overlap.
  * Returns PKA_ERR_INVALID_ARG for a NULL code_out or limit_us outside
  * [1, 2000000], PKA_ERR_CUDA on a launch or copy failure, else PKA_OK (also
  * when the wait timed out: that is reported through *code_out).
