@@ -53,3 +53,23 @@ def quantize(x, scale: float) -> np.ndarray:
 def dequantize(codes, scale: float) -> np.ndarray:
     """code value * scale, float64."""
     return decode(codes) * scale
+
+
+def codes_to_bf16_bits(codes) -> np.ndarray:
+    """bf16 bit patterns of the codes' values. Exact: every E4M3 value (3
+    mantissa bits, exponents 2^-9 .. 2^8) is a bf16 value; NaN stays NaN."""
+    v = decode(codes).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def attention_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, query_start_loc, seq_lens, scale,
+                  block_size, **kw):
+    """Attention over an 8-bit cache with per-tensor scales: K = k_scale x code,
+    V = v_scale x code. The scales come out of the sums (the score scale
+    becomes scale x k_scale, the output is multiplied by v_scale, the LSE
+    does not change), so the plain definition in `pka_oracle.c` runs on the
+    codes' exact bf16 values. Returns (out, lse) like `oracle.attention`."""
+    from . import attention
+    out, lse = attention(q, codes_to_bf16_bits(k_codes), codes_to_bf16_bits(v_codes), block_table,
+                         query_start_loc, seq_lens, scale * k_scale, block_size, **kw)
+    return out * v_scale, lse

@@ -60,3 +60,48 @@ def test_scaled_round_trip_error_bound():
     normal = np.abs(x / scale) >= 2.0 ** -6
     rel = np.abs(y[normal] - x[normal]) / np.abs(x[normal])
     assert rel.max() <= 2.0 ** -4 + 1e-12
+
+
+def test_codes_have_exact_bf16_values():
+    from paged_kv_attention_07_gb300 import workloads as W
+    codes = np.arange(256)
+    v = W.bf16_bits_to_f32(fp8.codes_to_bf16_bits(codes)).astype(np.float64)
+    ref = fp8.decode(codes)
+    assert np.array_equal(np.isnan(v), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(v[fin], ref[fin])
+
+
+def test_fp8_cache_attention_matches_dense_float64():
+    """An 8-bit cache (codes of the batch's K/V with per-tensor scales) through
+    the oracle against torch SDPA on the dequantized dense K/V."""
+    import oracle
+    from paged_kv_attention_07_gb300 import workloads as W
+    spec = W.spec_custom("fp8", ctx=[9, 40, 0], qlen=[1, 6, 5], num_decodes=1, num_extends=1,
+                         num_prefills=1, Hq=4, Hkv=2, d=16, dv=16, bs=8, seed=12)
+    batch = W.make_batch(spec)
+    kc, vc = oracle.populate_cache(batch, "all")
+    k_scale, v_scale = 0.0137, 0.0211  # arbitrary, not powers of two
+    fin = lambda bits: W.bf16_bits_to_f32(bits).astype(np.float64)
+    k_codes = fp8.quantize(np.nan_to_num(fin(kc)), k_scale)
+    v_codes = fp8.quantize(np.nan_to_num(fin(vc)), v_scale)
+    out, lse = fp8.attention_fp8(batch.q, k_codes, v_codes, k_scale, v_scale, batch.block_table,
+                                 batch.query_start_loc, batch.seq_lens, spec.scale, spec.block_size)
+    # dense reference on the dequantized values, request by request
+    G = spec.num_q_heads // spec.num_kv_heads
+    kd, vd = fp8.dequantize(k_codes, k_scale), fp8.dequantize(v_codes, v_scale)
+    rows = []
+    for r in range(spec.num_reqs):
+        t0, t1 = int(batch.query_start_loc[r]), int(batch.query_start_loc[r + 1])
+        S, ctx = int(batch.seq_lens[r]), spec.ctx[r]
+        blocks = batch.block_table[r]
+        K = np.stack([kd[blocks[j // spec.block_size], :, j % spec.block_size] for j in range(S)], 1)
+        V = np.stack([vd[blocks[j // spec.block_size], :, j % spec.block_size] for j in range(S)], 1)
+        q = torch.from_numpy(W.bf16_bits_to_f32(batch.q[t0:t1]).astype(np.float64)).permute(1, 0, 2)
+        Kt = torch.from_numpy(K).repeat_interleave(G, 0)
+        Vt = torch.from_numpy(V).repeat_interleave(G, 0)
+        mask = torch.arange(S)[None, :] <= ctx + torch.arange(t1 - t0)[:, None]
+        o = torch.nn.functional.scaled_dot_product_attention(q, Kt, Vt, attn_mask=mask, scale=spec.scale)
+        rows.append(o.permute(1, 0, 2).reshape(-1, spec.head_dim_v).numpy())
+    np.testing.assert_allclose(out, np.concatenate(rows), rtol=0, atol=1e-12)
+    assert np.isfinite(lse).all()
