@@ -12,8 +12,9 @@ prefill, mixed and MLA workloads are timed after it and reported under
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-For N > 1 launch with torch.distributed.run: every rank runs its own batch
-(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+For N > 1 (started by torch.distributed.run, or by this script itself when
+it was not) every rank runs its own batch (weak scaling, no collective on the
+data path); rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -483,6 +484,17 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def launch_ranks(n: int, argv) -> int:
+    """Run this script as n ranks under torch.distributed.run; returns its exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -498,6 +510,10 @@ def main():
                     help="short run for profilers: no clock hold, e2e, CPU baseline or secondary workloads")
     args = ap.parse_args()
     args.clock_hold = True
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not launched by torch.distributed.run: start the N ranks here (one
+        # process per GPU, rendezvous on the loopback address)
+        sys.exit(launch_ranks(args.gpus, sys.argv[1:]))
     if args.profile:
         args.e2e = args.all_workloads = args.cpu_baseline = args.clock_hold = False
     if args.warmup < 3:

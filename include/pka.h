@@ -236,8 +236,11 @@ PKA_API pka_status pka_get_error(const void *workspace, int32_t *code_out, void 
  * dim 128, up to about 2000 decode requests fit).
  *
  * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture. Every call on a device shares the one array, which keeps the last
+ * device current) and caches it for the rest of the process; make that first
+ * call before any stream capture. The cached address belongs to the device's
+ * primary context as it was at that first call: after cudaDeviceReset (or
+ * anything else that destroys that context) it is stale, so do not call this
+ * entry point again in that process. Every call on a device shares the one array, which keeps the last
  * call's contents (the call clears what must start at zero), so calls whose
  * work overlaps on the GPU -- on different streams, or from different host
  * threads -- race and must be serialised by the caller.

@@ -302,7 +302,9 @@ static pka_status check_shape(int nd, int ne, int np, int T, int Hq, int Hkv, in
         return PKA_ERR_INVALID_ARG;
     const int B = nd + ne + np;
     if (B > kMaxRequests) return PKA_ERR_UNSUPPORTED;
-    if ((int64_t)T < (int64_t)nd + 2LL * ne + np) return PKA_ERR_INVALID_ARG;
+    // every request owns at least one new token (an extend may hold just one:
+    // the single-path routing puts decodes there); the planner checks the real lengths
+    if ((int64_t)T < (int64_t)nd + ne + np) return PKA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return PKA_ERR_INVALID_ARG;
     if (maxs < maxq) return PKA_ERR_INVALID_ARG;
     if (chunk < 16) return PKA_ERR_INVALID_ARG;

@@ -11,13 +11,59 @@
 
 namespace pka {
 
+// Exclusive prefix sum of count(i) over i in [0, n), spread over the whole
+// block: each thread takes a contiguous run of indices, the runs' totals are
+// scanned with warp shuffles and one shared-memory pass. emit(i, first, count)
+// is called once per index with its exclusive offset. Returns the total to
+// every thread. All threads must call it (it synchronises the block); `scan`
+// holds at least 33 ints. Counts and the total must fit an int.
+template <typename CountF, typename EmitF>
+__device__ int scan_ranges(int n, int32_t* scan, CountF count, EmitF emit) {
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + nthr - 1) / nthr;
+    const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+    int local = 0;
+    for (int i = i0; i < i1; ++i) local += count(i);
+    int incl = local;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nthr >> 5;
+        int w = lane < nw ? scan[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += v;
+        }
+        if (lane < nw) scan[lane] = wi - w;  // exclusive offset of each warp
+        if (lane == 31) scan[32] = wi;       // total (lanes past nw added 0)
+    }
+    __syncthreads();
+    int off = scan[warp] + incl - local;
+    for (int i = i0; i < i1; ++i) {
+        const int c = count(i);
+        emit(i, off, c);
+        off += c;
+    }
+    const int total = scan[32];
+    __syncthreads();  // `scan` may be reused by the next call
+    return total;
+}
+
 __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
     __shared__ int32_t s_qlen[kMaxRequests];
     __shared__ int32_t s_slen[kMaxRequests];
     __shared__ int32_t s_hist[kCostBuckets];
     __shared__ int32_t s_err;
     __shared__ unsigned long long s_dec_keys;
-    __shared__ int32_t s_split, s_pairs, s_items, s_rows;
+    __shared__ int32_t s_split;
+    __shared__ int32_t s_scan[33];
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int nd = p.num_decodes, ne = p.num_extends;
@@ -70,7 +116,8 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
         return;
     }
 
-    // ---- decode split length and pair offsets (serial scan over smem)
+    // ---- decode split length (one thread), then every request's first pair
+    // and first extend partial row by block-wide prefix sums
     if (tid == 0) {
         int L = p.dec_min_split;
         if (nd > 0) {
@@ -80,27 +127,25 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
             want = (want + a - 1) / a * a;
             if (want > (unsigned long long)L) L = (int)(want > (1ull << 30) ? (1ull << 30) : want);
         }
-        int pairs = 0;
-        for (int r = 0; r < nd; ++r) {
-            const int n = (s_slen[r] + L - 1) / L;
-            p.dec_first[r] = pairs;
-            p.dec_nsplit[r] = n;
-            pairs += n;
-        }
-        int rows = 0;
-        for (int r = nd; r < nd + ne; ++r) {
-            const int ctx = s_slen[r] - s_qlen[r];
-            const int nslot = 1 + (ctx + p.chunk - 1) / p.chunk;
-            p.ext_base[r - nd] = rows;
-            rows += s_qlen[r] * nslot;
-        }
         s_split = L;
-        s_pairs = pairs;
-        s_rows = rows;
     }
     __syncthreads();
     const int L = s_split;
-    if (s_pairs > p.dec_pair_cap || s_rows > p.ext_row_cap) {
+    // decode request r has ceil(seq_len / L) splits
+    const int pairs = scan_ranges(nd, s_scan, [&](int r) { return (s_slen[r] + L - 1) / L; },
+                                  [&](int r, int first, int n) {
+                                      p.dec_first[r] = first;
+                                      p.dec_nsplit[r] = n;
+                                  });
+    // extend request r has qlen * (1 + chunks) partial rows
+    const int rows = scan_ranges(ne, s_scan,
+                                 [&](int i) {
+                                     const int r = nd + i;
+                                     const int ctx = s_slen[r] - s_qlen[r];
+                                     return s_qlen[r] * (1 + (ctx + p.chunk - 1) / p.chunk);
+                                 },
+                                 [&](int i, int first, int) { p.ext_base[i] = first; });
+    if (pairs > p.dec_pair_cap || rows > p.ext_row_cap) {
         if (tid == 0) {
             atomicOr(&p.hdr->err, PKA_DEVERR_CAPACITY);
             p.hdr->dec_num_pairs = 0;
@@ -141,17 +186,9 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
         for (int s = 0; s < nslot; ++s) atomicAdd(&s_hist[group_cost(r, s)], nqt);
     }
     __syncthreads();
-    if (tid == 0) {
-        int acc = 0;
-        for (int c = kCostBuckets - 1; c >= 0; --c) {  // descending cost
-            const int n = s_hist[c];
-            s_hist[c] = acc;
-            acc += n;
-        }
-        s_items = acc;
-    }
-    __syncthreads();
-    const int n_items = s_items;
+    // bucket offsets in descending cost: an exclusive scan over the reversed histogram
+    const int n_items = scan_ranges(kCostBuckets, s_scan, [&](int i) { return s_hist[kCostBuckets - 1 - i]; },
+                                    [&](int i, int first, int) { s_hist[kCostBuckets - 1 - i] = first; });
     if (n_items > p.fa_item_cap) {
         if (tid == 0) {
             atomicOr(&p.hdr->err, PKA_DEVERR_CAPACITY);
@@ -176,11 +213,11 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
     }
     if (tid == 0) {
         p.hdr->dec_split_len = L;
-        p.hdr->dec_num_pairs = s_pairs;
+        p.hdr->dec_num_pairs = pairs;
         p.hdr->fa_num_items = n_items;
         p.hdr->dec_counter = 0;
         p.hdr->fa_counter = 0;
-        p.hdr->ext_rows = s_rows;
+        p.hdr->ext_rows = rows;
     }
 }
 

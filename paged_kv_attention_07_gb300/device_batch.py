@@ -19,6 +19,23 @@ def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
 
 
+GUARD_BYTES = 4096  # canary bytes before and after each output and the workspace
+CANARY = 0xA5
+
+
+def guarded_empty(nbytes: int, device) -> tuple[torch.Tensor, torch.Tensor]:
+    """A zeroed uint8 buffer of nbytes with GUARD_BYTES of CANARY on both sides
+    (the offset keeps the start 256-byte aligned). Returns (whole, inner)."""
+    buf = torch.full((GUARD_BYTES + nbytes + GUARD_BYTES,), CANARY, dtype=torch.uint8, device=device)
+    inner = buf[GUARD_BYTES:GUARD_BYTES + nbytes]
+    inner.zero_()
+    return buf, inner
+
+
+def canary_intact(buf: torch.Tensor) -> bool:
+    return bool(torch.all(buf[:GUARD_BYTES] == CANARY)) and bool(torch.all(buf[-GUARD_BYTES:] == CANARY))
+
+
 class DeviceBatch:
     def __init__(self, batch: W.Batch, device="cuda", values_on_device_seed: int | None = None,
                  unified: bool = False):
@@ -63,15 +80,57 @@ class DeviceBatch:
                                 self.k_cache, self.v_cache)
             del kc, vc
         del k_seq, v_seq
-        self.out = torch.zeros((T, Hq, dv), dtype=torch.bfloat16, device=device)
-        self.lse = torch.zeros((T, Hq), dtype=torch.float32, device=device)
+        # out, lse and the workspace sit between canary bytes: a store past
+        # either end of them shows up in canaries_intact()
+        self._out_buf, inner = guarded_empty(T * Hq * dv * 2, device)
+        self.out = inner.view(torch.bfloat16).view(T, Hq, dv)
+        self._lse_buf, inner = guarded_empty(T * Hq * 4, device)
+        self.lse = inner.view(torch.float32).view(T, Hq)
         self.max_query_len = int(max(spec.qlen))
         self.max_seq_len = int(max(spec.seq_lens))
         ws = pka.pka_workspace_size(*self.counts, T, Hq, Hkv, d, dv, self.max_query_len, self.max_seq_len,
                                     spec.context_chunk)
         if ws == 0:
             raise RuntimeError("pka_workspace_size rejected the batch shape")
-        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
+        self._ws_buf, self.workspace = guarded_empty(ws, device)
+        torch.cuda.synchronize()
+
+    def canaries_intact(self) -> bool:
+        """True when no byte next to out, lse or the workspace was written."""
+        torch.cuda.synchronize()
+        return all(canary_intact(b) for b in (self._out_buf, self._lse_buf, self._ws_buf))
+
+    def refill(self, batch: W.Batch):
+        """Write another batch with the same request counts and token count, and
+        lengths within this one's hints, into the same device buffers (what a
+        server does between replays of a captured step): metadata, Q, the new
+        tokens' K/V, and the cache (poisoned again, then the new context rows)."""
+        s, spec = self.spec, batch.spec
+        assert (spec.num_decodes, spec.num_extends, spec.num_prefills) == (
+            s.num_decodes, s.num_extends, s.num_prefills)
+        assert spec.num_tokens == s.num_tokens and batch.num_blocks <= self.k_cache.shape[0]
+        assert max(spec.qlen) <= self.max_query_len and max(spec.seq_lens) <= self.max_seq_len
+        assert batch.block_table.shape[1] <= self.block_table.shape[1]
+        dev = self.device
+        bt = np.zeros(tuple(self.block_table.shape), dtype=np.int32)
+        bt[:, : batch.block_table.shape[1]] = batch.block_table
+        self.block_table.copy_(torch.from_numpy(bt))
+        self.qsl.copy_(torch.from_numpy(batch.query_start_loc))
+        self.seq_lens.copy_(torch.from_numpy(batch.seq_lens))
+        self.slot_mapping.copy_(torch.from_numpy(np.ascontiguousarray(batch.slot_mapping)))
+        self.q.copy_(bf16_tensor(batch.q, dev))
+        self.k_new.copy_(bf16_tensor(batch.k_new, dev))
+        if self.v_new is not None:
+            self.v_new.copy_(bf16_tensor(batch.v_new, dev))
+        self.k_cache.fill_(float("nan"))
+        if self.v_cache is not None:
+            self.v_cache.fill_(float("nan"))
+        if batch.ctx_index.size:
+            ci = batch.ctx_index
+            kc = bf16_tensor(batch.k_seq[ci], dev)
+            vc = None if batch.v_seq is None else bf16_tensor(batch.v_seq[ci], dev)
+            pka.pka_cache_write(kc, vc, torch.from_numpy(batch.slot_all[ci]).to(dev), self.k_cache, self.v_cache)
+        self.batch = batch
         torch.cuda.synchronize()
 
     def cache_write(self, stream=None):

@@ -197,8 +197,13 @@ def pka_gather_rows(dst, src, index, error_word=None, stream=None):
         return
     if not (dst.is_contiguous() and src.is_contiguous() and index.is_contiguous()):
         raise ValueError("pka_gather_rows: dst, src and index must be contiguous (packed rows)")
-    if dst.dtype != src.dtype or dst[0].numel() != src[0].numel() or index.dtype.itemsize != 4:
-        raise ValueError("pka_gather_rows: dst and src rows must match; index must be int32")
+    import torch
+    if dst.dtype != src.dtype or dst[0].numel() != src[0].numel():
+        raise ValueError("pka_gather_rows: dst and src rows must match")
+    if index.dtype != torch.int32:
+        raise ValueError("pka_gather_rows: index must be int32")
+    if not (dst.is_cuda and src.is_cuda and index.is_cuda) or len({dst.device, src.device, index.device}) != 1:
+        raise ValueError("pka_gather_rows: dst, src and index must be CUDA tensors on one device")
     if index.numel() < dst.shape[0]:
         raise ValueError("pka_gather_rows: index shorter than dst")
     row_bytes = dst[0].numel() * dst.element_size()

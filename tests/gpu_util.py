@@ -16,6 +16,7 @@ def run_gpu(batch, values_on_device_seed=None):
     db = DeviceBatch(batch, values_on_device_seed=values_on_device_seed)
     db.step()
     torch.cuda.synchronize()
+    assert db.canaries_intact(), "a kernel wrote past out, lse or the workspace"
     err = db.error_word()
     dv = batch.spec.head_dim_v
     out = db.out.float().cpu().numpy().reshape(-1, dv)

@@ -37,7 +37,7 @@ def test_shuffled_batch_through_order_and_gather(seed):
     assert eo <= OUT_ATOL and el <= LSE_ATOL, (eo, el)
 
 
-@pytest.mark.parametrize("width", [4, 1024])  # 16-byte rows (flat loop), 4 KB rows (a warp per row)
+@pytest.mark.parametrize("width", [4, 1024])  # 16-byte rows and 4 KB rows, both through the flat (row, copy) loop
 def test_gather_rows_bad_index_zero_fills_and_flags(width):
     src = torch.arange(10 * width, dtype=torch.float32, device="cuda").view(10, width)
     idx = torch.tensor([3, -1, 9, 10], dtype=torch.int32, device="cuda")
@@ -61,13 +61,8 @@ def test_gather_rows_widths(row_bytes):
     assert torch.equal(dst, src[idx.long()])
 
 
-def test_step_replays_from_a_cuda_graph():
-    spec = W.spec_custom("graph", ctx=[3, 700, 40, 1500, 0, 0], qlen=[1, 1, 33, 70, 100, 7], num_decodes=2,
-                         num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=128, dv=128, bs=16, chunk=512, seed=7)
-    db = DeviceBatch(W.make_batch(spec))
-    db.step()
-    torch.cuda.synchronize()
-    ref_out, ref_lse = db.out.clone(), db.lse.clone()
+def _graph_of_step(db):
+    """Capture db.step() (cache write + forward) in a CUDA graph."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -76,6 +71,17 @@ def test_step_replays_from_a_cuda_graph():
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         db.step()
+    return graph
+
+
+def test_step_replays_from_a_cuda_graph():
+    spec = W.spec_custom("graph", ctx=[3, 700, 40, 1500, 0, 0], qlen=[1, 1, 33, 70, 100, 7], num_decodes=2,
+                         num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=128, dv=128, bs=16, chunk=512, seed=7)
+    db = DeviceBatch(W.make_batch(spec))
+    db.step()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = db.out.clone(), db.lse.clone()
+    graph = _graph_of_step(db)
     db.out.zero_()
     db.lse.zero_()
     graph.replay()
@@ -83,3 +89,38 @@ def test_step_replays_from_a_cuda_graph():
     torch.cuda.synchronize()
     assert db.error_word() == 0
     assert torch.equal(db.out, ref_out) and torch.equal(db.lse, ref_lse)
+
+
+def test_graph_replays_new_metadata():
+    """What a serving loop does with a captured step: each replay gets a new
+    batch written into the same buffers (other lengths, block table, slots, Q
+    and K/V; same request counts and token count, lengths within the host
+    hints the graph was captured with). Every replay must match the oracle of
+    the batch it was given."""
+    common = dict(num_decodes=2, num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=128, dv=128, bs=16, chunk=512)
+    first = W.spec_custom("graph_a", ctx=[3, 700, 40, 1500, 0, 0], qlen=[1, 1, 33, 70, 100, 7], seed=8, **common)
+    db = DeviceBatch(W.make_batch(first))
+    graph = _graph_of_step(db)
+    nb = db.k_cache.shape[0]
+    later = [  # 212 new tokens each, like the captured batch
+        W.spec_custom("graph_b", ctx=[650, 12, 1400, 90, 0, 0], qlen=[1, 1, 50, 53, 60, 47], seed=9,
+                      num_blocks=nb, **common),
+        W.spec_custom("graph_c", ctx=[1, 1, 1, 1, 0, 0], qlen=[1, 1, 2, 98, 99, 11], seed=10, num_blocks=nb,
+                      **common),
+    ]
+    for spec in [first] + later:
+        batch = W.make_batch(spec)
+        if spec is not first:
+            db.refill(batch)
+        db.out.fill_(float("nan"))
+        db.lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert db.error_word() == 0, spec.name
+        assert db.canaries_intact(), spec.name
+        ref_o, ref_l = oracle.batch_reference(batch)
+        o = db.out.float().cpu().numpy().reshape(-1, spec.head_dim_v)
+        l = db.lse.cpu().numpy().reshape(-1)
+        assert np.isfinite(o).all() and np.isfinite(l).all(), spec.name
+        eo, el = np.abs(o - ref_o).max(), np.abs(l - ref_l).max()
+        assert eo <= OUT_ATOL and el <= LSE_ATOL, (spec.name, eo, el)

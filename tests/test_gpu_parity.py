@@ -324,3 +324,23 @@ def test_decodes_routed_through_the_extend_path(bs):
     torch.cuda.synchronize()
     assert db.error_word() == 0
     compare(batch, db.out.float().cpu().numpy().reshape(-1, spec.head_dim_v), db.lse.cpu().numpy().reshape(-1))
+
+
+def test_unified_routing_mostly_one_token_requests():
+    """Single-path routing of a decode-heavy batch: 64 one-token requests and
+    one 4-token extend all in the extend slice, so the extend slice holds
+    fewer than two new tokens per request."""
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    rng = np.random.default_rng(21)
+    ctx = rng.integers(1, 3000, 64).tolist()
+    spec = W.spec_custom("unified_dec", ctx=ctx + [500], qlen=[1] * 64 + [4], num_decodes=64, num_extends=1,
+                         num_prefills=0, Hq=32, Hkv=4, d=128, dv=128, bs=16, chunk=1024, seed=21)
+    batch = W.make_batch(spec)
+    db = DeviceBatch(batch, unified=True)
+    assert db.counts == (0, 65, 0)
+    db.step()
+    import torch
+    torch.cuda.synchronize()
+    assert db.error_word() == 0
+    assert db.canaries_intact()
+    compare(batch, db.out.float().cpu().numpy().reshape(-1, spec.head_dim_v), db.lse.cpu().numpy().reshape(-1))
