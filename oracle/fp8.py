@@ -50,6 +50,18 @@ def quantize(x, scale: float) -> np.ndarray:
     return encode(np.asarray(x, dtype=np.float64) / scale)
 
 
+def quantize_f32(x, scale: float) -> np.ndarray:
+    """Codes of the float32 quotient x / scale: x and scale are float32 values,
+    the division is IEEE float32 (round to nearest even), and that quotient is
+    encoded. This is where the code is decided for the 8-bit cache write, so
+    both the kernel and this reference take the decision in float32 (the
+    pages fix no precision for the scale division)."""
+    xf = np.asarray(x, dtype=np.float32)
+    with np.errstate(over="ignore"):
+        qf = xf / np.float32(scale)
+    return encode(qf.astype(np.float64))
+
+
 def dequantize(codes, scale: float) -> np.ndarray:
     """code value * scale, float64."""
     return decode(codes) * scale

@@ -105,3 +105,26 @@ def test_fp8_cache_attention_matches_dense_float64():
         rows.append(o.permute(1, 0, 2).reshape(-1, spec.head_dim_v).numpy())
     np.testing.assert_allclose(out, np.concatenate(rows), rtol=0, atol=1e-12)
     assert np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("scale", [0.0125, 0.02, 1.0 / 3.0, 7.0])
+def test_float32_quotient_codes_match_torch(scale):
+    # torch divides two float32 tensors in float32 and casts the quotient to
+    # float8_e4m3fn (round to nearest even): in range, the same codes
+    rng = np.random.default_rng(int(scale * 1000))
+    x = (rng.standard_normal(20000) * 3.0).astype(np.float32)
+    q = torch.from_numpy(x) / torch.tensor(scale, dtype=torch.float32)
+    keep = (q.abs() <= fp8.MAX_FINITE).numpy()
+    ref = q[torch.from_numpy(keep)].to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(fp8.quantize_f32(x, scale)[keep], ref)
+
+
+def test_float32_quotient_differs_from_exact_only_at_double_rounding():
+    # the float32 quotient can land exactly on a midpoint the exact quotient
+    # misses; away from such cases the two encodings agree
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(50000)).astype(np.float32)
+    s = 0.0123
+    a, b = fp8.quantize_f32(x, s), fp8.quantize(x.astype(np.float64), np.float64(np.float32(s)))
+    assert (a != b).sum() <= 5
+    assert np.all(np.abs(fp8.decode(a) - fp8.decode(b))[a != b] <= 2.0 ** -3 * np.abs(fp8.decode(b))[a != b] + 2 ** -9)
