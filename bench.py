@@ -40,11 +40,13 @@ METRIC = "decode KV GB/s & tokens/s; prefill/extend TFLOPS; % of HBM / BF16 roof
 
 
 # ---------------------------------------------------------------- work model
-def algorithmic_work(spec: W.BatchSpec) -> dict:
-    """Bytes and flops a step must move/do, counted once (no re-reads)."""
+def algorithmic_work(spec: W.BatchSpec, kv_elem_bytes: int = 2) -> dict:
+    """Bytes and flops a step must move/do, counted once (no re-reads).
+    kv_elem_bytes: bytes per cache element (2 = bf16, 1 = the 8-bit cache)."""
     Hq, Hkv, d, dv = spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.head_dim_v
     nd, ne = spec.num_decodes, spec.num_extends
-    row_bytes = (d * 2) if spec.mla else Hkv * (d + dv) * 2  # one key's K+V (latent: one row)
+    e = kv_elem_bytes
+    row_bytes = (d * e) if spec.mla else Hkv * (d + dv) * e  # one key's K+V (latent: one row)
     dec_keys = sum(spec.seq_lens[:nd])
     dec_bytes = dec_keys * row_bytes
     dec_flops = dec_keys * Hq * 2 * (d + dv)
@@ -54,7 +56,8 @@ def algorithmic_work(spec: W.BatchSpec) -> dict:
         q, c = spec.qlen[r], spec.ctx[r]
         ext_pairs += q * c + q * (q + 1) // 2
     pre_pairs = sum(q * (q + 1) // 2 for q in spec.qlen[nd + ne:])
-    cw_bytes = 2 * spec.num_tokens * row_bytes  # read + write
+    # read (bf16 K/V rows) + write (cache elements)
+    cw_bytes = spec.num_tokens * (Hkv * (d + (0 if spec.mla else dv)) * 2 + row_bytes)
     return {"dec_bytes": dec_bytes, "dec_flops": dec_flops, "ext_flops": ext_pairs * pair_flops,
             "pre_flops": pre_pairs * pair_flops, "cache_write_bytes": cw_bytes,
             "tokens": spec.num_tokens, "decode_tokens": nd}
@@ -148,10 +151,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm
-def make_device_batch(spec, device, seed, unified=False):
+FP8_SCALES = (0.0125, 0.02)  # per-tensor K / V scales of the 8-bit cache workloads
+
+
+def make_device_batch(spec, device, seed, unified=False, kv_scales=None):
     from paged_kv_attention_07_gb300.device_batch import DeviceBatch
     batch = W.make_batch(spec, values=False)
-    return DeviceBatch(batch, device=device, values_on_device_seed=seed, unified=unified)
+    return DeviceBatch(batch, device=device, values_on_device_seed=seed, unified=unified, kv_scales=kv_scales)
 
 
 def time_steps(db, steps, warmup, flush_bytes=0, kernels=(), barrier=None):
@@ -234,7 +240,9 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
     import torch
     res = {}
     # (name, spec, dominant kernel, bound, L2 flush bytes, committed ncu traffic entry)
-    cases = [("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20,
+    cases = [("decode_gqa_fp8", W.spec_decode_gqa(), "decode", "hbm", 0,
+              ("decode_gqa_fp8.cu", "decode_gqa_fp8")),
+             ("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20,
               ("fa_fwd.cu", "fa_fwd_prefill_varlen")),
              ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0, ("fa_fwd.cu", "fa_fwd_mixed")),
              ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0,
@@ -242,11 +250,18 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
              ("mla_decode_bs1", W.spec_mla_decode(block_size=1), "decode", "hbm", 0, None)]
     for name, spec, dom, bound, flush, tkey in cases:
         traffic = kernel_traffic(*tkey) if tkey else None
-        db = make_device_batch(spec, device, seed=1234 + rank)
+        fp8 = name.endswith("_fp8")
+        db = make_device_batch(spec, device, seed=1234 + rank, kv_scales=FP8_SCALES if fp8 else None)
         ms, stats, launches, _ = time_steps(db, steps, warmup, flush_bytes=flush)
-        w = algorithmic_work(spec)
+        w = algorithmic_work(spec, 1 if fp8 else 2)
         ent = {"ms_per_step": round(ms, 4), "tokens_per_s": round(w["tokens"] / (ms * 1e-3), 1),
                "kernels": {k: round(v["avg_ms"], 4) for k, v in stats.items()}}
+        if fp8:
+            ent["cache"] = f"FP8 E4M3 codes, k_scale {FP8_SCALES[0]}, v_scale {FP8_SCALES[1]}"
+        cw = stats.get("cache_write", {}).get("avg_ms")
+        if cw:  # the step's cache write: its own bytes (read + write), its own roofline
+            ent["cache_write"] = roofline("hbm", w["cache_write_bytes"] / (cw * 1e-3) / 1e9, peaks["hbm_gbs"],
+                                          "GB/s", None)
         kms = stats.get(dom, {}).get("avg_ms")
         if bound == "tensor":
             flops = w["ext_flops"] + w["pre_flops"]
@@ -411,6 +426,8 @@ def run_ours(args):
         "roofline": roofline("hbm", achieved, peaks["hbm_gbs"], "GB/s", traffic),
         "roofline_peak_source": peaks["source"],
         "kernels_ms": {k: round(v["avg_ms"], 4) for k, v in stats.items()},
+        "cache_write": (roofline("hbm", w["cache_write_bytes"] / (stats["cache_write"]["avg_ms"] * 1e-3) / 1e9,
+                                 peaks["hbm_gbs"], "GB/s", None) if "cache_write" in stats else None),
         "gpu_launches": launches,
         "clocks": clocks,
     }
@@ -434,7 +451,8 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "prefill_varlen": W.spec_prefill, "mixed": W.spec_mixed,
+WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "decode_gqa_fp8": W.spec_decode_gqa,
+             "prefill_varlen": W.spec_prefill, "mixed": W.spec_mixed,
              "mla_decode_bs64": W.spec_mla_decode,
              "mla_decode_bs1": lambda: W.spec_mla_decode(block_size=1),
              "mixed_unified": W.spec_mixed, "mixed_unordered": W.spec_mixed}
@@ -443,7 +461,8 @@ WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "prefill_varlen": W.spec_prefill, 
 def profile_workload(args, device):
     """Run --steps steps of one workload and print its timing (for profilers)."""
     spec = WORKLOADS[args.workload]()
-    db = make_device_batch(spec, device, seed=7, unified=args.workload == "mixed_unified")
+    db = make_device_batch(spec, device, seed=7, unified=args.workload == "mixed_unified",
+                           kv_scales=FP8_SCALES if args.workload.endswith("_fp8") else None)
     if args.workload == "mixed_unordered":
         import numpy as np
         from paged_kv_attention_07_gb300.device_batch import UnorderedBatch

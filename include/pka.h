@@ -105,6 +105,29 @@ PKA_API pka_status pka_cache_write(const void *k, const void *v, const int64_t *
                            int32_t *error_word, void *stream);
 
 /*
+ * pka_cache_write_fp8 -- pka_cache_write into an 8-bit cache: the pages'
+ * cache write with a quantising KV-cache dtype ("Beyond porting",
+ * non-absorbed recipe: the context is gathered from the cache and
+ * dequantised, gather_and_maybe_dequant_cache). Every element is stored as
+ * an FP8 E4M3 code ("fn" variant: bit 7 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, no infinities, 0x7F/0xFF = NaN, largest finite 448) of one
+ * tensor-wide scale per cache:
+ *     k_cache[s / bs][h][s % bs][i] = E4M3(k[t][h][i] / k_scale)
+ * and likewise v with v_scale. The quotient is formed in float32 (IEEE
+ * round to nearest) and rounded to the nearest code, ties to the even code;
+ * finite quotients beyond +-448 saturate to +-448. Same arguments, layouts,
+ * slot rules and error behaviour as pka_cache_write, except:
+ *   k_cache, v_cache  device, [num_blocks, num_kv_heads, block_size, head_dim(_v)]
+ *                     uint8 codes, 16-byte aligned; both required (no latent cache)
+ *   k_scale, v_scale  finite and > 0, else PKA_ERR_INVALID_ARG
+ * head_dim and head_dim_v must be multiples of 8 with head_dim + head_dim_v <= 1024.
+ */
+PKA_API pka_status pka_cache_write_fp8(const void *k, const void *v, const int64_t *slot_mapping,
+                                       int64_t num_tokens, int num_kv_heads, int head_dim, int head_dim_v,
+                                       void *k_cache, void *v_cache, int64_t num_blocks, int block_size,
+                                       float k_scale, float v_scale, int32_t *error_word, void *stream);
+
+/*
  * pka_workspace_size -- bytes of scratch pka_paged_attn_forward needs for a
  * batch described by the same host hints (see pka_paged_attn_forward). The
  * result depends on the current device's SM count. Never fails; returns 0
@@ -180,6 +203,38 @@ PKA_API pka_status pka_paged_attn_forward(const void *q, const void *k_new, cons
                                   int context_chunk_tokens, int max_query_len, int max_seq_len,
                                   void *out, float *lse, void *workspace, size_t workspace_bytes,
                                   void *stream);
+
+/*
+ * pka_paged_attn_forward_fp8 -- pka_paged_attn_forward over an 8-bit cache
+ * written by pka_cache_write_fp8 (K = k_scale x code, V = v_scale x code).
+ *
+ * Computes the same definition with those K and V values:
+ *     s_j = scale * k_scale * <q[t][h], code_K[j]>,
+ *     out[t][h] = v_scale * sum_j softmax(s)_j code_V[j],   lse as before.
+ * The codes are widened inside the decode kernel's tile loads (every E4M3
+ * value is exactly an f16 value); the products run on f16 operands with
+ * float32 accumulation, so q is converted to f16 once per work unit: the call
+ * requires |q| < 65504 (larger magnitudes saturate) and rounds q elements
+ * below 2^-14 in magnitude to f16's subnormal spacing 2^-24.
+ *
+ * Arguments as in pka_paged_attn_forward, with k_cache / v_cache as uint8 E4M3
+ * codes in the same [num_blocks, num_kv_heads, block_size, head_dim] layout and
+ * the two scales (finite, > 0). The workspace is sized by the same
+ * pka_workspace_size. Supported: decode-only batches (num_extends ==
+ * num_prefills == 0), head_dim == head_dim_v == 128, v_cache not NULL,
+ * num_q_heads / num_kv_heads <= 16, block_size a power of two in [1, 128];
+ * other shapes return PKA_ERR_UNSUPPORTED.
+ */
+PKA_API pka_status pka_paged_attn_forward_fp8(const void *q, const void *k_new, const void *v_new,
+                                              const void *k_cache, const void *v_cache,
+                                              const int32_t *block_table, int max_blocks_per_req,
+                                              const int32_t *query_start_loc, const int32_t *seq_lens,
+                                              int num_decodes, int num_extends, int num_prefills,
+                                              int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                                              int head_dim_v, int64_t num_blocks, int block_size, float scale,
+                                              float k_scale, float v_scale, int context_chunk_tokens,
+                                              int max_query_len, int max_seq_len, void *out, float *lse,
+                                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * pka_merge_attn_states -- combine two partial attention results over

@@ -16,7 +16,10 @@ namespace pka {
 cudaError_t launch_planner(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_cache_write(const void* k, const void* v, const int64_t* slots, int64_t T, int Hkv,
                                int d, int dv, void* k_cache, void* v_cache, int64_t num_blocks, int bs,
-                               int32_t* err, int num_sms, cudaStream_t stream);
+                               int32_t* err, int num_sms, cudaStream_t stream, bool fp8, float k_scale,
+                               float v_scale);
+cudaError_t launch_decode_gqa_fp8(const CUtensorMap& km, const CUtensorMap& vm, const DecodeGqaParams& p, bool tma,
+                                  int num_sms, cudaStream_t stream);
 cudaError_t launch_merge_pair(void* out, float* out_lse, const void* a, const float* a_lse, const void* b,
                               const float* b_lse, int64_t rows, int dv, int io_dtype, int num_sms,
                               cudaStream_t stream);
@@ -90,6 +93,20 @@ bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D byte view [rows, 128] (8-bit cache rows of 128 codes) read in boxes
+// of 128 bytes x box_rows rows with the 128-byte swizzle.
+bool encode_rows_u8(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -292,7 +309,31 @@ pka_status pka_cache_write(const void* k, const void* v, const int64_t* slot_map
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(timed(PKA_KERNEL_CACHE_WRITE, st, [&] {
         return launch_cache_write(k, v, slot_mapping, num_tokens, num_kv_heads, head_dim, head_dim_v, k_cache,
-                                  v_cache, num_blocks, block_size, error_word, sms, st);
+                                  v_cache, num_blocks, block_size, error_word, sms, st, false, 1.f, 1.f);
+    }));
+}
+
+pka_status pka_cache_write_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                               int num_kv_heads, int head_dim, int head_dim_v, void* k_cache, void* v_cache,
+                               int64_t num_blocks, int block_size, float k_scale, float v_scale, int32_t* error_word,
+                               void* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim_v <= 0 || num_blocks <= 0 ||
+        block_size <= 0)
+        return PKA_ERR_INVALID_ARG;
+    if (!std::isfinite(k_scale) || !(k_scale > 0.f) || !std::isfinite(v_scale) || !(v_scale > 0.f))
+        return PKA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKA_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0 || head_dim_v % 8 != 0 || (head_dim + head_dim_v) / 8 > 128) return PKA_ERR_UNSUPPORTED;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8) || (error_word && !aligned(error_word, 4)))
+        return PKA_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return PKA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(timed(PKA_KERNEL_CACHE_WRITE, st, [&] {
+        return launch_cache_write(k, v, slot_mapping, num_tokens, num_kv_heads, head_dim, head_dim_v, k_cache,
+                                  v_cache, num_blocks, block_size, error_word, sms, st, true, k_scale, v_scale);
     }));
 }
 
@@ -337,14 +378,23 @@ size_t pka_workspace_size(int num_decodes, int num_extends, int num_prefills, in
     return L.total;
 }
 
-pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                  const void* v_cache, const int32_t* block_table, int max_blocks_per_req,
-                                  const int32_t* query_start_loc, const int32_t* seq_lens, int num_decodes,
-                                  int num_extends, int num_prefills, int num_tokens, int num_q_heads,
-                                  int num_kv_heads, int head_dim, int head_dim_v, int64_t num_blocks,
-                                  int block_size, float scale, int context_chunk_tokens, int max_query_len,
-                                  int max_seq_len, void* out, float* lse, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The cache's element format: bf16, or E4M3 codes with one scale per tensor.
+struct CacheFormat {
+    bool fp8;
+    float k_scale, v_scale;
+};
+
+pka_status forward_impl(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                        const void* v_cache, const int32_t* block_table, int max_blocks_per_req,
+                        const int32_t* query_start_loc, const int32_t* seq_lens, int num_decodes, int num_extends,
+                        int num_prefills, int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                        int head_dim_v, int64_t num_blocks, int block_size, float scale, int context_chunk_tokens,
+                        int max_query_len, int max_seq_len, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream, const CacheFormat& cf) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int B = num_decodes + num_extends + num_prefills;
     if (B == 0 && num_tokens == 0) return PKA_OK;
@@ -355,6 +405,13 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
                                 head_dim, head_dim_v, max_query_len, max_seq_len, context_chunk_tokens, mla,
                                 &is_mla);
     if (sc != PKA_OK) return sc;
+    if (cf.fp8) {
+        // the 8-bit cache: GQA decode-only batches of head dim 128
+        if (is_mla || head_dim != 128 || head_dim_v != 128) return PKA_ERR_UNSUPPORTED;
+        if (num_extends + num_prefills > 0) return PKA_ERR_UNSUPPORTED;
+        if (!std::isfinite(cf.k_scale) || !(cf.k_scale > 0.f) || !std::isfinite(cf.v_scale) || !(cf.v_scale > 0.f))
+            return PKA_ERR_INVALID_ARG;
+    }
     if (B < 1) return PKA_ERR_INVALID_ARG;
     if (!q || !k_cache || !block_table || !query_start_loc || !seq_lens || !out || !workspace)
         return PKA_ERR_INVALID_ARG;
@@ -461,14 +518,19 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
             std::memset(&vm, 0, sizeof(vm));
             if (tma) {
                 const uint32_t br = (uint32_t)std::min(block_size, 16);
-                if (!encode_rows(&km, k_cache, (uint64_t)cache_rows, head_dim, br) ||
-                    !encode_rows(&vm, v_cache, (uint64_t)cache_rows, head_dim, br))
-                    return PKA_ERR_CUDA;
+                const bool ok = cf.fp8 ? (encode_rows_u8(&km, k_cache, (uint64_t)cache_rows, br) &&
+                                          encode_rows_u8(&vm, v_cache, (uint64_t)cache_rows, br))
+                                       : (encode_rows(&km, k_cache, (uint64_t)cache_rows, head_dim, br) &&
+                                          encode_rows(&vm, v_cache, (uint64_t)cache_rows, head_dim, br));
+                if (!ok) return PKA_ERR_CUDA;
             }
             DecodeGqaParams dp;
             dp.q = static_cast<const __nv_bfloat16*>(q);
             dp.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
             dp.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+            dp.k8 = static_cast<const uint8_t*>(k_cache);
+            dp.v8 = static_cast<const uint8_t*>(v_cache);
+            dp.v_scale = cf.fp8 ? cf.v_scale : 1.f;
             dp.block_table = block_table;
             dp.seq_lens = seq_lens;
             dp.hdr = hdr;
@@ -486,9 +548,12 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
             dp.Hkv = num_kv_heads;
             dp.G = num_q_heads / num_kv_heads;
             dp.bs = block_size;
-            dp.scale_log2 = scale_log2;
-            if ((e = timed(PKA_KERNEL_DECODE, st,
-                           [&] { return launch_decode_gqa(km, vm, dp, head_dim, tma, sms, st); })) != cudaSuccess)
+            // 8-bit cache: a score is scale * k_scale * <q, code>
+            dp.scale_log2 = cf.fp8 ? scale_log2 * cf.k_scale : scale_log2;
+            if ((e = timed(PKA_KERNEL_DECODE, st, [&] {
+                     return cf.fp8 ? launch_decode_gqa_fp8(km, vm, dp, tma, sms, st)
+                                   : launch_decode_gqa(km, vm, dp, head_dim, tma, sms, st);
+                 })) != cudaSuccess)
                 return PKA_ERR_CUDA;
         }
         DecodeReduceParams rp;
@@ -576,6 +641,39 @@ pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* 
         }
     }
     return PKA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pka_status pka_paged_attn_forward(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table, int max_blocks_per_req,
+                                  const int32_t* query_start_loc, const int32_t* seq_lens, int num_decodes,
+                                  int num_extends, int num_prefills, int num_tokens, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int head_dim_v, int64_t num_blocks,
+                                  int block_size, float scale, int context_chunk_tokens, int max_query_len,
+                                  int max_seq_len, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    return forward_impl(q, k_new, v_new, k_cache, v_cache, block_table, max_blocks_per_req, query_start_loc,
+                        seq_lens, num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads,
+                        head_dim, head_dim_v, num_blocks, block_size, scale, context_chunk_tokens, max_query_len,
+                        max_seq_len, out, lse, workspace, workspace_bytes, stream, CacheFormat{false, 1.f, 1.f});
+}
+
+pka_status pka_paged_attn_forward_fp8(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_table, int max_blocks_per_req,
+                                      const int32_t* query_start_loc, const int32_t* seq_lens, int num_decodes,
+                                      int num_extends, int num_prefills, int num_tokens, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int head_dim_v, int64_t num_blocks,
+                                      int block_size, float scale, float k_scale, float v_scale,
+                                      int context_chunk_tokens, int max_query_len, int max_seq_len, void* out,
+                                      float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    return forward_impl(q, k_new, v_new, k_cache, v_cache, block_table, max_blocks_per_req, query_start_loc,
+                        seq_lens, num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads,
+                        head_dim, head_dim_v, num_blocks, block_size, scale, context_chunk_tokens, max_query_len,
+                        max_seq_len, out, lse, workspace, workspace_bytes, stream,
+                        CacheFormat{true, k_scale, v_scale});
 }
 
 pka_status pka_merge_attn_states(void* out, float* out_lse, const void* prefix_out, const float* prefix_lse,
@@ -707,6 +805,9 @@ pka_status pka_paged_decode_noalloc(const void* q, const void* k_cache, const vo
     dp.q = static_cast<const __nv_bfloat16*>(q);
     dp.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
     dp.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+    dp.k8 = nullptr;
+    dp.v8 = nullptr;
+    dp.v_scale = 1.f;
     dp.block_table = block_table;
     dp.seq_lens = seq_lens;
     dp.hdr = hdr;

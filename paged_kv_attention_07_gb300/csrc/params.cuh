@@ -15,6 +15,9 @@ struct DecodeGqaParams {
     const __nv_bfloat16* q;        // [T, Hq, D]
     const __nv_bfloat16* k_cache;  // [nb, Hkv, bs, D]
     const __nv_bfloat16* v_cache;
+    const uint8_t* k8;             // the same caches as E4M3 codes (8-bit cache kernel)
+    const uint8_t* v8;
+    float v_scale;                 // 8-bit cache: value of one V code unit (the output's factor)
     const int32_t* block_table;
     const int32_t* seq_lens;
     const PlanHeader* hdr;

@@ -36,11 +36,19 @@ def canary_intact(buf: torch.Tensor) -> bool:
     return bool(torch.all(buf[:GUARD_BYTES] == CANARY)) and bool(torch.all(buf[-GUARD_BYTES:] == CANARY))
 
 
+FP8_NAN = 0x7F  # an E4M3 NaN code: the poison of an 8-bit cache
+
+
 class DeviceBatch:
+    """kv_scales=(k_scale, v_scale) makes the caches 8-bit (E4M3 codes with one
+    scale per tensor): written by pka_cache_write_fp8, read by
+    pka_paged_attn_forward_fp8."""
+
     def __init__(self, batch: W.Batch, device="cuda", values_on_device_seed: int | None = None,
-                 unified: bool = False):
+                 unified: bool = False, kv_scales: tuple[float, float] | None = None):
         spec = batch.spec
         self.batch, self.spec, self.device = batch, spec, device
+        self.kv_scales = kv_scales
         # unified: the decodes go in the extend slice (num_decodes 0), so every
         # request with context runs through the extend path
         nd = 0 if unified else spec.num_decodes
@@ -54,9 +62,14 @@ class DeviceBatch:
         self.block_table = torch.from_numpy(batch.block_table).to(device)
         self.slot_mapping = torch.from_numpy(np.ascontiguousarray(batch.slot_mapping)).to(device)
         nb = batch.num_blocks
-        self.k_cache = torch.full((nb, Hkv, bs, d), float("nan"), dtype=torch.bfloat16, device=device)
-        self.v_cache = None if spec.mla else torch.full((nb, Hkv, bs, dv), float("nan"),
-                                                        dtype=torch.bfloat16, device=device)
+        if kv_scales is None:
+            self.k_cache = torch.full((nb, Hkv, bs, d), float("nan"), dtype=torch.bfloat16, device=device)
+            self.v_cache = None if spec.mla else torch.full((nb, Hkv, bs, dv), float("nan"),
+                                                            dtype=torch.bfloat16, device=device)
+        else:
+            assert not spec.mla, "the 8-bit cache holds separate K and V"
+            self.k_cache = torch.full((nb, Hkv, bs, d), FP8_NAN, dtype=torch.uint8, device=device)
+            self.v_cache = torch.full((nb, Hkv, bs, dv), FP8_NAN, dtype=torch.uint8, device=device)
         if values_on_device_seed is None:
             self.q = bf16_tensor(batch.q, device)
             k_seq = bf16_tensor(batch.k_seq, device)
@@ -76,8 +89,7 @@ class DeviceBatch:
         if ctx_idx.numel():
             kc = k_seq.index_select(0, ctx_idx).contiguous()
             vc = None if v_seq is None else v_seq.index_select(0, ctx_idx).contiguous()
-            pka.pka_cache_write(kc, vc, slot_all.index_select(0, ctx_idx).contiguous(),
-                                self.k_cache, self.v_cache)
+            self._write(kc, vc, slot_all.index_select(0, ctx_idx).contiguous())
             del kc, vc
         del k_seq, v_seq
         # out, lse and the workspace sit between canary bytes: a store past
@@ -122,23 +134,36 @@ class DeviceBatch:
         self.k_new.copy_(bf16_tensor(batch.k_new, dev))
         if self.v_new is not None:
             self.v_new.copy_(bf16_tensor(batch.v_new, dev))
-        self.k_cache.fill_(float("nan"))
+        poison = float("nan") if self.kv_scales is None else FP8_NAN
+        self.k_cache.fill_(poison)
         if self.v_cache is not None:
-            self.v_cache.fill_(float("nan"))
+            self.v_cache.fill_(poison)
         if batch.ctx_index.size:
             ci = batch.ctx_index
             kc = bf16_tensor(batch.k_seq[ci], dev)
             vc = None if batch.v_seq is None else bf16_tensor(batch.v_seq[ci], dev)
-            pka.pka_cache_write(kc, vc, torch.from_numpy(batch.slot_all[ci]).to(dev), self.k_cache, self.v_cache)
+            self._write(kc, vc, torch.from_numpy(batch.slot_all[ci]).to(dev))
         self.batch = batch
         torch.cuda.synchronize()
 
+    def _write(self, k, v, slots, stream=None):
+        if self.kv_scales is None:
+            pka.pka_cache_write(k, v, slots, self.k_cache, self.v_cache, stream=stream)
+        else:
+            pka.pka_cache_write_fp8(k, v, slots, self.k_cache, self.v_cache, *self.kv_scales, stream=stream)
+
     def cache_write(self, stream=None):
-        pka.pka_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
-                            stream=stream)
+        self._write(self.k_new, self.v_new, self.slot_mapping, stream=stream)
 
     def forward(self, stream=None, out=None, lse=None):
         s = self.spec
+        if self.kv_scales is not None:
+            pka.pka_paged_attn_forward_fp8(
+                self.q, self.k_new, self.v_new, self.k_cache, self.v_cache, self.block_table, self.qsl,
+                self.seq_lens, *self.counts, s.scale, *self.kv_scales, s.context_chunk, self.max_query_len,
+                self.max_seq_len, self.out if out is None else out, self.lse if lse is None else lse,
+                self.workspace, stream=stream)
+            return
         pka.pka_paged_attn_forward(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
                                    self.block_table, self.qsl, self.seq_lens, *self.counts, s.scale,
                                    s.context_chunk,

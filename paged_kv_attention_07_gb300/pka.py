@@ -19,7 +19,8 @@ STATUS_NAMES = {0: "PKA_OK", 1: "PKA_ERR_INVALID_ARG", 2: "PKA_ERR_UNSUPPORTED",
 DEVERR = {"QUERY_START_LOC": 0x01, "SEQ_LEN": 0x02, "ORDER": 0x04, "QUERY_LEN": 0x08,
           "BLOCK_TABLE": 0x10, "BLOCK_ID": 0x20, "SLOT": 0x40, "CAPACITY": 0x80, "TIMEOUT": 0x100,
           "INDEX": 0x200}
-EXPORTED = ("pka_cache_write", "pka_workspace_size", "pka_paged_attn_forward",
+EXPORTED = ("pka_cache_write", "pka_cache_write_fp8", "pka_workspace_size", "pka_paged_attn_forward",
+            "pka_paged_attn_forward_fp8",
             "pka_merge_attn_states", "pka_get_error", "pka_paged_decode_noalloc", "pka_kernel_timer",
             "pka_kernel_timer_read", "pka_batch_order", "pka_gather_rows", "pka_selftest_wait",
             "pka_status_string")
@@ -53,6 +54,11 @@ def load(path: str | None = None):
     P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
     lib.pka_cache_write.restype = i32
     lib.pka_cache_write.argtypes = [P, P, P, i64, i32, i32, i32, P, P, i64, i32, P, P]
+    lib.pka_cache_write_fp8.restype = i32
+    lib.pka_cache_write_fp8.argtypes = [P, P, P, i64, i32, i32, i32, P, P, i64, i32, f32, f32, P, P]
+    lib.pka_paged_attn_forward_fp8.restype = i32
+    lib.pka_paged_attn_forward_fp8.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                               i32, i32, i64, i32, f32, f32, f32, i32, i32, i32, P, P, P, sz, P]
     lib.pka_workspace_size.restype = sz
     lib.pka_workspace_size.argtypes = [i32] * 11
     lib.pka_paged_attn_forward.restype = i32
@@ -112,6 +118,17 @@ def pka_cache_write(k, v, slot_mapping, k_cache, v_cache, error_word=None, strea
     _check(st, "pka_cache_write")
 
 
+def pka_cache_write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, error_word=None, stream=None):
+    """k [T, Hkv, d], v [T, Hkv, dv] bf16; caches [nb, Hkv, bs, d(v)] uint8 E4M3 codes."""
+    T, Hkv, d = k.shape
+    dv = v.shape[2]
+    nb, _, bs, _ = k_cache.shape
+    st = load().pka_cache_write_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, d, dv, _ptr(k_cache),
+                                    _ptr(v_cache), nb, bs, float(k_scale), float(v_scale), _ptr(error_word),
+                                    _stream(stream))
+    _check(st, "pka_cache_write_fp8")
+
+
 def pka_workspace_size(num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads,
                        head_dim, head_dim_v, max_query_len, max_seq_len, context_chunk_tokens) -> int:
     return int(load().pka_workspace_size(num_decodes, num_extends, num_prefills, num_tokens, num_q_heads,
@@ -136,6 +153,22 @@ def pka_paged_attn_forward(q, k_new, v_new, k_cache, v_cache, block_table, query
         max_seq_len, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check(st, "pka_paged_attn_forward")
+
+
+def pka_paged_attn_forward_fp8(q, k_new, v_new, k_cache, v_cache, block_table, query_start_loc, seq_lens,
+                               num_decodes, num_extends, num_prefills, scale, k_scale, v_scale,
+                               context_chunk_tokens, max_query_len, max_seq_len, out, lse, workspace, stream=None):
+    """pka_paged_attn_forward over uint8 E4M3 caches with per-tensor scales."""
+    T, Hq, d = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    dv = out.shape[2]
+    st = load().pka_paged_attn_forward_fp8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens), num_decodes, num_extends,
+        num_prefills, T, Hq, Hkv, d, dv, nb, bs, float(scale), float(k_scale), float(v_scale),
+        context_chunk_tokens, max_query_len, max_seq_len, _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pka_paged_attn_forward_fp8")
 
 
 def pka_merge_attn_states(out, out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse, stream=None):

@@ -115,3 +115,25 @@ def test_selftest_wait_rejects_bad_arguments(lib, limit_us, with_code):
     code = ctypes.c_int32(0)
     st = lib.pka_selftest_wait(0, limit_us, ctypes.byref(code) if with_code else None, None)
     assert st == 1  # PKA_ERR_INVALID_ARG, before any CUDA call
+
+
+def test_fp8_entry_points_reject_bad_arguments(lib):
+    # cache write: bad scales, missing V, head_dim not a multiple of 8
+    cw = lambda **kw: lib.pka_cache_write_fp8(
+        kw.get("k", FAKE), kw.get("v", FAKE), FAKE, 4, 2, kw.get("d", 128), 128, FAKE, kw.get("vc", FAKE), 8, 16,
+        ctypes.c_float(kw.get("ks", 0.5)), ctypes.c_float(kw.get("vs", 0.5)), None, None)
+    assert cw(ks=0.0) == 1 and cw(vs=float("nan")) == 1 and cw(ks=-1.0) == 1
+    assert cw(v=None) == 1 and cw(vc=None) == 1
+    assert cw(d=60) == 2
+
+    def fwd(**kw):
+        a = dict(nd=2, ne=0, np=0, T=2, d=128, dv=128, ks=0.5, vs=0.5, vc=FAKE)
+        a.update(kw)
+        return lib.pka_paged_attn_forward_fp8(
+            FAKE, FAKE, FAKE, FAKE, a["vc"], FAKE, 8, FAKE, FAKE, a["nd"], a["ne"], a["np"], a["T"], 8, 2, a["d"],
+            a["dv"], 64, 16, ctypes.c_float(0.125), ctypes.c_float(a["ks"]), ctypes.c_float(a["vs"]), 32, 4, 100,
+            FAKE, None, P(0x100000), 1 << 20, None)
+    assert fwd(ne=1, T=6) == 2          # extend over an 8-bit cache: no kernel
+    assert fwd(np=1, T=6) == 2          # prefill likewise
+    assert fwd(d=64, dv=64) == 2        # head dim 64
+    assert fwd(ks=0.0) == 1 and fwd(vs=float("inf")) == 1

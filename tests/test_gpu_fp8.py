@@ -1,0 +1,134 @@
+"""GPU parity of the 8-bit (FP8 E4M3) KV cache: the quantising cache write
+bit for bit against the oracle's codes (float32 quotient, nearest code, ties
+to even, saturation), and the decode over the codes against the oracle's
+attention on the codes' exact values with the scales taken out of the sums."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import fp8
+from paged_kv_attention_07_gb300 import workloads as W
+from tests.gpu_util import LSE_ATOL, OUT_ATOL
+
+pytestmark = pytest.mark.gpu
+
+K_SCALE, V_SCALE = 0.0125, 0.02
+
+
+def _codes_of(bits, scale):
+    return fp8.quantize_f32(W.bf16_bits_to_f32(bits), scale)
+
+
+def oracle_fp8_cache(batch, k_scale, v_scale):
+    """The oracle's 8-bit caches after the step's cache write: every position
+    (context and new tokens) quantised, every other slot the NaN code."""
+    kc, vc = oracle.populate_cache(batch, "all")
+    return _codes_of(kc, k_scale), _codes_of(vc, v_scale)
+
+
+def run_fp8(batch, k_scale=K_SCALE, v_scale=V_SCALE):
+    import torch
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    db = DeviceBatch(batch, kv_scales=(k_scale, v_scale))
+    db.step()
+    torch.cuda.synchronize()
+    assert db.canaries_intact()
+    return db
+
+
+def check_fp8(batch, k_scale=K_SCALE, v_scale=V_SCALE):
+    db = run_fp8(batch, k_scale, v_scale)
+    assert db.error_word() == 0
+    kc, vc = oracle_fp8_cache(batch, k_scale, v_scale)
+    # the cache the kernel read is exactly the oracle's codes
+    assert np.array_equal(db.k_cache.cpu().numpy(), kc)
+    assert np.array_equal(db.v_cache.cpu().numpy(), vc)
+    spec = batch.spec
+    ref_o, ref_l = fp8.attention_fp8(batch.q, kc, vc, k_scale, v_scale, batch.block_table, batch.query_start_loc,
+                                     batch.seq_lens, spec.scale, spec.block_size, head_dim_v=spec.head_dim_v)
+    out = db.out.float().cpu().numpy().reshape(-1, spec.head_dim_v)
+    lse = db.lse.cpu().numpy().reshape(-1)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    eo, el = np.abs(out - ref_o).max(), np.abs(lse - ref_l).max()
+    assert eo <= OUT_ATOL and el <= LSE_ATOL, (eo, el)
+    return eo, el
+
+
+DEC_CTX = [0, 1, 15, 16, 17, 255, 256, 257, 600, 1500, 4100]
+
+
+@pytest.mark.parametrize("bs", [1, 2, 4, 8, 16, 64, 128])
+def test_fp8_decode_block_sizes(bs):
+    spec = W.spec_custom(f"f8_bs{bs}", ctx=DEC_CTX, qlen=[1] * len(DEC_CTX), num_decodes=len(DEC_CTX),
+                         num_extends=0, num_prefills=0, Hq=32, Hkv=4, d=128, dv=128, bs=bs, seed=100 + bs)
+    check_fp8(W.make_batch(spec))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (32, 4), (32, 2), (6, 3)])
+def test_fp8_decode_groups(Hq, Hkv):
+    spec = W.spec_custom(f"f8_g{Hq // Hkv}", ctx=DEC_CTX, qlen=[1] * len(DEC_CTX), num_decodes=len(DEC_CTX),
+                         num_extends=0, num_prefills=0, Hq=Hq, Hkv=Hkv, d=128, dv=128, bs=16, seed=200 + Hq)
+    check_fp8(W.make_batch(spec))
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.004, 0.05)])
+def test_fp8_decode_scales(k_scale, v_scale):
+    # scale 1: N(0,1) values use few codes; 0.004: many values saturate at 448
+    spec = W.spec_custom("f8_sc", ctx=[30, 700, 2500], qlen=[1, 1, 1], num_decodes=3, num_extends=0,
+                         num_prefills=0, Hq=16, Hkv=2, d=128, dv=128, bs=16, seed=7)
+    check_fp8(W.make_batch(spec), k_scale, v_scale)
+
+
+def test_fp8_decode_config_shape():
+    """Every row of the decode-only GQA workload (256 requests, context
+    U[1024, 8192], 32 query / 4 KV heads, head dim 128, block 16)."""
+    check_fp8(W.make_batch(W.spec_decode_gqa()))
+
+
+def test_fp8_cache_write_rounding_cases():
+    """Hand-placed values: exact ties (to the even code), saturation, values
+    below half the smallest subnormal, signed zero, a skipped (negative) slot
+    and an out-of-range slot (flagged, skipped)."""
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    s = 0.5  # a power of two: x / s is exact, so the ties below are real ties
+    vals = np.array([1.0625, 1.1875, -1.0625, 500.0, -2.0 ** 20, 2.0 ** -10, 3 * 2.0 ** -10, 0.0, -0.0, 448.0,
+                     464.0, 2.0 ** -11, 1.0, -2.5, 0.375, 7.0], np.float32) * np.float32(s)
+    T, Hkv, d = 4, 1, 16
+    x = np.tile(vals, (T, Hkv, 1)).astype(np.float32)
+    x[1] *= -1
+    bits = W.to_bf16_bits(x)
+    assert np.array_equal(W.bf16_bits_to_f32(bits), x)  # every value is a bf16 value
+    nb, bs = 4, 2
+    slots = np.array([0, 5, -1, nb * bs + 1], np.int64)
+    kc = torch.full((nb, Hkv, bs, d), 0x7F, dtype=torch.uint8, device="cuda")
+    vc = torch.full((nb, Hkv, bs, d), 0x7F, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kt = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    pka.pka_cache_write_fp8(kt, kt, torch.from_numpy(slots).cuda(), kc, vc, s, 2 * s, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pka.DEVERR["SLOT"]
+    ref_k = np.full((nb, Hkv, bs, d), 0x7F, np.uint8)
+    ref_v = ref_k.copy()
+    for t in range(2):
+        blk, off = divmod(int(slots[t]), bs)
+        ref_k[blk, 0, off] = fp8.quantize_f32(x[t, 0], s)
+        ref_v[blk, 0, off] = fp8.quantize_f32(x[t, 0], 2 * s)
+    assert np.array_equal(kc.cpu().numpy(), ref_k)
+    assert np.array_equal(vc.cpu().numpy(), ref_v)
+    # the first row's codes, spelled out: ties to even, saturation, subnormal ties, signed zero
+    assert ref_k[0, 0, 0, :12].tolist() == [0x38, 0x3A, 0xB8, 0x7E, 0xFE, 0x00, 0x02, 0x00, 0x80, 0x7E, 0x7E, 0x00]
+
+
+def test_fp8_forward_rejects_unsupported():
+    """Shapes the 8-bit path has no kernel for are refused before any launch."""
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    spec = W.spec_custom("f8_ext", ctx=[10, 40], qlen=[1, 5], num_decodes=1, num_extends=1, num_prefills=0,
+                         Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=32, seed=3)
+    db = DeviceBatch(W.make_batch(spec), kv_scales=(K_SCALE, V_SCALE))
+    with pytest.raises(pka.PkaError) as ei:
+        db.forward()
+    assert ei.value.status == 2
+    torch.cuda.synchronize()
