@@ -245,6 +245,8 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
              ("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20,
               ("fa_fwd.cu", "fa_fwd_prefill_varlen")),
              ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0, ("fa_fwd.cu", "fa_fwd_mixed")),
+             ("mla_prefill_extend", W.spec_mla_prefill(), "prefill_extend", "tensor", 0,
+              ("fa_fwd.cu", "fa_fwd_mla_prefill_extend")),
              ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0,
               ("decode_mla_tc.cu", "decode_mla_tc_mla_decode_bs64")),
              ("mla_decode_bs1", W.spec_mla_decode(block_size=1), "decode", "hbm", 0, None)]
@@ -453,7 +455,7 @@ def run_ours(args):
 
 WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "decode_gqa_fp8": W.spec_decode_gqa,
              "prefill_varlen": W.spec_prefill, "mixed": W.spec_mixed,
-             "mla_decode_bs64": W.spec_mla_decode,
+             "mla_decode_bs64": W.spec_mla_decode, "mla_prefill_extend": W.spec_mla_prefill,
              "mla_decode_bs1": lambda: W.spec_mla_decode(block_size=1),
              "mixed_unified": W.spec_mixed, "mixed_unordered": W.spec_mixed}
 

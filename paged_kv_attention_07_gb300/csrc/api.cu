@@ -28,7 +28,8 @@ cudaError_t launch_decode_gqa(const CUtensorMap& km, const CUtensorMap& vm, cons
                               int head_dim, bool tma, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode_mla(const CUtensorMap& map, const DecodeMlaParams& p, bool tma, int num_sms,
                               cudaStream_t stream);
-cudaError_t launch_fa_fwd(const FaMaps& maps, const FaParams& p, int head_dim, int num_sms, cudaStream_t stream);
+cudaError_t launch_fa_fwd(const FaMaps& maps, const FaParams& p, int head_dim, int head_dim_v, int num_sms,
+                          cudaStream_t stream);
 cudaError_t launch_decode_reduce(const DecodeReduceParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t num_rows, int64_t src_rows,
                                int64_t row_bytes, int32_t* err, int num_sms, cudaStream_t stream);
@@ -354,7 +355,11 @@ static pka_status check_shape(int nd, int ne, int np, int T, int Hq, int Hkv, in
         if (!(Hq == 16 || Hq == 32 || Hq % 64 == 0)) return PKA_ERR_UNSUPPORTED;
         if (ne + np > 0) return PKA_ERR_UNSUPPORTED;
     } else {
-        if (!((d == 64 || d == 128) && dv == d)) return PKA_ERR_UNSUPPORTED;
+        // (192, 128): the non-absorbed MLA prefill/extend (K = 128 nope + 64 rope
+        // dims, V = 128); the split-KV decode has no kernel for it
+        const bool nonabsorbed = d == 192 && dv == 128;
+        if (!(((d == 64 || d == 128) && dv == d) || nonabsorbed)) return PKA_ERR_UNSUPPORTED;
+        if (nonabsorbed && nd > 0) return PKA_ERR_UNSUPPORTED;
         if (Hq / Hkv > 16) return PKA_ERR_UNSUPPORTED;
     }
     *is_mla = mla;
@@ -616,7 +621,7 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
                 return PKA_ERR_CUDA;
         }
         if ((e = timed(PKA_KERNEL_PREFILL_EXTEND, st,
-                       [&] { return launch_fa_fwd(maps, fp, head_dim, sms, st); })) != cudaSuccess)
+                       [&] { return launch_fa_fwd(maps, fp, head_dim, head_dim_v, sms, st); })) != cudaSuccess)
             return PKA_ERR_CUDA;
         if (num_extends > 0) {
             ExtendReduceParams xp;

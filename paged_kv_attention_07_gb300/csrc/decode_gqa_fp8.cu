@@ -5,10 +5,16 @@
 // step). Decode is bound by the cache bytes it streams, so an 8-bit cache
 // halves its time; the codes are widened on the fly, never written back.
 //
-// Same work decomposition, pipeline and softmax as decode_gqa.cu (unit =
-// (request, split, kv head); each warp a private ring of 16-key tiles loaded
-// by TMA straight through the block table; warps merged in shared memory).
-// Head dim 128. What differs is how the MMA fragments are built:
+// Work unit (request, split, kv head), as in decode_gqa.cu, but a whole unit
+// belongs to one warp: each warp takes units from the planner's counter on
+// its own, streams the unit's 16-key tiles through a private ring loaded by
+// TMA straight through the block table, and writes the unit's result from
+// registers -- no shared-memory merge and no block-wide barrier, so a warp
+// never waits for another. The ring runs across unit boundaries: the warp
+// knows its next unit one unit ahead and starts loading its tiles while the
+// current unit's last tiles are consumed. (With half the bytes per key, the
+// per-unit costs of the bf16 kernel's CTA-wide units would no longer hide
+// behind the stream.) Head dim 128. How the MMA fragments are built:
 //
 //   * Every E4M3 value is exactly an f16 value (4-bit exponent, 3-bit
 //     mantissa, subnormals down to 2^-9), so the tensor-core products run on
@@ -39,14 +45,22 @@ namespace {
 
 constexpr int kF8Warps = 4;
 constexpr int kF8Threads = kF8Warps * 32;
-constexpr int kF8Stages = 6;           // tiles in flight per warp
 constexpr int kF8Tile = 16;            // keys per tile
 constexpr int kF8D = 128;              // head dim (bytes per cache row)
 constexpr int kF8TileBytes = kF8Tile * kF8D;       // 2 KB
 constexpr int kF8StageBytes = 2 * kF8TileBytes;    // K + V
-constexpr int kF8RingBytes = kF8Warps * kF8Stages * kF8StageBytes;
-constexpr int kF8Smem = kF8RingBytes + 1024 + 64 * 8;
-static_assert(kF8Warps * 16 * kF8D * 4 + 2 * kF8Warps * 16 * 4 <= kF8RingBytes, "merge scratch fits the ring");
+
+// Per head-group width NT (8 query heads per 8-wide MMA column block): tiles
+// in flight per warp and CTAs per SM. One group (G <= 8) keeps 16 warps per
+// SM (four 48 KB CTAs, registers capped at 128) so the warps' dependent MMA /
+// softmax chains hide each other; two groups need more registers per thread.
+template <int NT>
+struct F8Cfg {
+    static constexpr int kStages = NT == 1 ? 3 : 6;
+    static constexpr int kMinBlocks = NT == 1 ? 4 : 2;
+    static constexpr int kRingBytes = kF8Warps * kStages * kF8StageBytes;
+    static constexpr int kSmem = kRingBytes + 1024 + 64 * 8;
+};
 
 // Two E4M3 codes (low byte -> low half) to an f16 pair.
 PKA_DEVICE uint32_t e4m3x2_to_f16x2(uint32_t x16) {
@@ -88,16 +102,61 @@ PKA_DEVICE uint4 lds128(uint32_t addr) {
 
 }  // namespace
 
+// One decode work unit as a warp sees it. blk[0] / blk[1]: validated block
+// ids of the unit's TMA boxes `lane` and 32 + lane (a box is min(bs, 16) rows
+// of one block), loaded when the unit is fetched, so issuing a tile's loads
+// only shuffles them out of registers.
+struct F8Unit {
+    int unit, pair, g, r, k0, k1, ntiles;  // unit < 0: none
+    int blk[2];
+};
+
+PKA_DEVICE int f8_block_id(const DecodeGqaParams& p, const int32_t* bt, int pos) {
+    int blk = __ldg(bt + pos / p.bs);
+    if (blk < 0 || blk >= p.num_blocks) {
+        set_error(p.err, PKA_DEVERR_BLOCK_ID);
+        blk = 0;
+    }
+    return blk;
+}
+
+// Call with the whole warp (the unit index is warp-uniform).
+PKA_DEVICE F8Unit f8_unit(const DecodeGqaParams& p, int u, int num_units, int L, int lane) {
+    F8Unit U;
+    U.unit = -1;
+    U.ntiles = 0;
+    U.blk[0] = U.blk[1] = 0;
+    if (u < 0 || u >= num_units) return U;
+    U.unit = u;
+    U.pair = u / p.Hkv;
+    U.g = u - U.pair * p.Hkv;
+    const int2 rs = p.pairs[U.pair];
+    U.r = rs.x;
+    U.k0 = rs.y * L;
+    U.k1 = min(U.k0 + L, p.seq_lens[U.r]);
+    U.ntiles = U.k1 > U.k0 ? (U.k1 - U.k0 + kF8Tile - 1) / kF8Tile : 0;
+    if (p.bs >= 8) {
+        const int boxr = p.bs < kF8Tile ? p.bs : kF8Tile;
+        const int32_t* bt = p.block_table + (int64_t)U.r * p.max_blocks;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int pos = U.k0 + (32 * i + lane) * boxr;
+            if (pos < U.k1) U.blk[i] = f8_block_id(p, bt, pos);
+        }
+    }
+    return U;
+}
+
 template <int NT, bool kTma>
-__global__ void __launch_bounds__(kF8Threads, 2)
+__global__ void __launch_bounds__(kF8Threads, F8Cfg<NT>::kMinBlocks)
     decode_gqa_fp8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const DecodeGqaParams p) {
     constexpr int kKSteps = kF8D / 16;
+    constexpr int kF8Stages = F8Cfg<NT>::kStages;
+    constexpr int kF8RingBytes = F8Cfg<NT>::kRingBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kF8RingBytes);
-    __shared__ int s_unit;
-    __shared__ int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c4 = lane & 3, r8 = lane >> 2;
@@ -109,35 +168,106 @@ __global__ void __launch_bounds__(kF8Threads, 2)
     if (lane == 0) {
         for (int s = 0; s < kF8Stages; ++s) mbar_init(&full[s], kTma ? 1 : 32);
         fence_barrier_init();
-    }
-    if (threadIdx.x == 0) {
-        s_abort = 0;
-        if (kTma) {
+        if (kTma && warp == 0) {
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
         }
     }
-    __syncthreads();
+    __syncwarp();
+    // From here on every warp runs on its own: it takes whole units from the
+    // counter and never synchronises with the other warps.
     const uint64_t pol = policy_evict_first();
     uint8_t* ring = smem + warp * kF8Stages * kF8StageBytes;
-    uint32_t ld_it = 0, cs_it = 0;  // tiles issued / consumed by this warp (all units)
-    bool alive = true;              // false once a wait of this warp timed out
+    uint32_t ld_it = 0, cs_it = 0;  // tiles issued / consumed by this warp
 
-    for (;;) {
-        if (threadIdx.x == 0) s_unit = s_abort ? num_units : atomicAdd(p.counter, 1);
-        __syncthreads();
-        const int unit = s_unit;
-        __syncthreads();
-        if (unit >= num_units) break;
-        const int pair = unit / p.Hkv, g = unit - pair * p.Hkv;
-        const int2 rs = p.pairs[pair];
-        const int r = rs.x, split = rs.y;
-        const int slen = p.seq_lens[r];
-        const int k0 = split * L;
-        const int k1 = min(k0 + L, slen);
-        const int ntiles = (k1 - k0 + kF8Tile - 1) / kF8Tile;
-        const int my_n = ntiles > warp ? (ntiles - warp + kF8Warps - 1) / kF8Warps : 0;
-        const int32_t* bt = p.block_table + (int64_t)r * p.max_blocks;
+    auto fetch = [&]() -> F8Unit {
+        int u = 0;
+        if (lane == 0) u = atomicAdd(p.counter, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        return f8_unit(p, u, num_units, L, lane);
+    };
+    F8Unit cur = fetch();
+    F8Unit nxt = cur.unit >= 0 ? fetch() : cur;
+    // load cursor: tile `lt` of cur (lw == 0) or of nxt (lw == 1)
+    int lw = 0, lt = 0;
+
+    // issue the next tile along the cursor into stage ld_it % kF8Stages;
+    // false when nothing can be issued yet (next unit not known or none)
+    auto issue_next = [&]() -> bool {
+        if (lw == 0 && lt >= cur.ntiles) {
+            lw = 1;
+            lt = 0;
+        }
+        // the cursor's unit, field by field (a reference to one of two structs
+        // would put both in local memory)
+        F8Unit U;
+        U.unit = lw ? nxt.unit : cur.unit;
+        U.ntiles = lw ? nxt.ntiles : cur.ntiles;
+        U.g = lw ? nxt.g : cur.g;
+        U.r = lw ? nxt.r : cur.r;
+        U.k0 = lw ? nxt.k0 : cur.k0;
+        U.k1 = lw ? nxt.k1 : cur.k1;
+        U.blk[0] = lw ? nxt.blk[0] : cur.blk[0];
+        U.blk[1] = lw ? nxt.blk[1] : cur.blk[1];
+        if (U.unit < 0 || lt >= U.ntiles) return false;
+        const int stage = ld_it % kF8Stages;
+        uint8_t* kdst = ring + stage * kF8StageBytes;
+        uint8_t* vdst = kdst + kF8TileBytes;
+        const int tb = U.k0 + lt * kF8Tile;
+        const int32_t* bt = p.block_table + (int64_t)U.r * p.max_blocks;
+        if constexpr (kTma) {
+            const int boxr = p.bs < kF8Tile ? p.bs : kF8Tile;
+            const int nsub = kF8Tile / boxr;  // 1 or 2 boxes per tile
+            // the tile's block ids: from the unit's registers (boxes < 64), else loaded
+            const int b0 = lt * nsub, b1 = b0 + nsub - 1;  // the tile's first and last box
+            int blk, blk1;
+            if (b1 < 64) {
+                blk = __shfl_sync(0xffffffffu, b0 < 32 ? U.blk[0] : U.blk[1], b0 & 31);
+                blk1 = __shfl_sync(0xffffffffu, b1 < 32 ? U.blk[0] : U.blk[1], b1 & 31);
+            } else {
+                blk = lane == 0 ? f8_block_id(p, bt, tb) : 0;
+                blk1 = (lane == 0 && nsub > 1 && tb + boxr < U.k1) ? f8_block_id(p, bt, tb + boxr) : 0;
+            }
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                const int nbox = (nsub > 1 && tb + boxr < U.k1) ? 2 : 1;
+                mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * nbox * boxr * kF8D));
+                for (int sb = 0; sb < nbox; ++sb) {
+                    const int ps = tb + sb * boxr;
+                    const int row = ((sb ? blk1 : blk) * p.Hkv + U.g) * p.bs + (ps % p.bs);
+                    tma_load_2d(kdst + sb * boxr * kF8D, &kmap, &full[stage], 0, row, pol);
+                    tma_load_2d(vdst + sb * boxr * kF8D, &vmap, &full[stage], 0, row, pol);
+                }
+            }
+            __syncwarp();
+        } else {
+            // 16-byte copies into the same swizzled layout: 16 rows x 8 pieces
+            const uint32_t kbase = smem_u32(kdst), vbase = smem_u32(vdst);
+            for (int ci = lane; ci < kF8Tile * 8; ci += 32) {
+                const int tr = ci >> 3, c = ci & 7;
+                const int pos = tb + tr;
+                if (pos >= U.k1) continue;
+                int blk = __ldg(bt + pos / p.bs);
+                if (blk < 0 || blk >= p.num_blocks) {
+                    set_error(p.err, PKA_DEVERR_BLOCK_ID);
+                    blk = 0;
+                }
+                const int64_t row = ((int64_t)blk * p.Hkv + U.g) * p.bs + (pos % p.bs);
+                cp_async_16(kbase + sw128(tr, c), p.k8 + row * kF8D + c * 16);
+                cp_async_16(vbase + sw128(tr, c), p.v8 + row * kF8D + c * 16);
+            }
+            cp_async_arrive_noinc(&full[stage]);
+        }
+        ++ld_it;
+        ++lt;
+        return true;
+    };
+
+    bool alive = true;  // false once a wait timed out: stop issuing and consuming
+    while (alive && cur.unit >= 0) {
+        while (ld_it - cs_it < (uint32_t)kF8Stages && issue_next()) {
+        }
+        const int r = cur.r, g = cur.g;
 
         // Q^T fragments (B operand, f16): head g*G + n (n = lane / 4), k-step ks
         // holds dims 32c + 4ks .. +3; zero beyond G.
@@ -158,54 +288,6 @@ __global__ void __launch_bounds__(kF8Threads, 2)
             }
         }
 
-        // issue the loads of this warp's j-th tile into stage (ld_it % kF8Stages)
-        auto issue = [&](int j) {
-            const int stage = ld_it % kF8Stages;
-            uint8_t* kdst = ring + stage * kF8StageBytes;
-            uint8_t* vdst = kdst + kF8TileBytes;
-            const int tb = k0 + (warp + j * kF8Warps) * kF8Tile;
-            if constexpr (kTma) {
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    const int boxr = p.bs < kF8Tile ? p.bs : kF8Tile;
-                    const int nsub = kF8Tile / boxr;
-                    int nbox = 0;
-                    for (int sb = 0; sb < nsub; ++sb)
-                        if (tb + sb * boxr < k1) ++nbox;
-                    mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * nbox * boxr * kF8D));
-                    for (int sb = 0; sb < nbox; ++sb) {
-                        const int pos = tb + sb * boxr;
-                        int blk = __ldg(bt + pos / p.bs);
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            set_error(p.err, PKA_DEVERR_BLOCK_ID);
-                            blk = 0;
-                        }
-                        const int row = (blk * p.Hkv + g) * p.bs + (pos % p.bs);
-                        tma_load_2d(kdst + sb * boxr * kF8D, &kmap, &full[stage], 0, row, pol);
-                        tma_load_2d(vdst + sb * boxr * kF8D, &vmap, &full[stage], 0, row, pol);
-                    }
-                }
-            } else {
-                // 16-byte copies into the same swizzled layout: 16 rows x 8 pieces
-                const uint32_t kbase = smem_u32(kdst), vbase = smem_u32(vdst);
-                for (int ci = lane; ci < kF8Tile * 8; ci += 32) {
-                    const int tr = ci >> 3, c = ci & 7;
-                    const int pos = tb + tr;
-                    if (pos >= k1) continue;
-                    int blk = __ldg(bt + pos / p.bs);
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        set_error(p.err, PKA_DEVERR_BLOCK_ID);
-                        blk = 0;
-                    }
-                    const int64_t row = ((int64_t)blk * p.Hkv + g) * p.bs + (pos % p.bs);
-                    cp_async_16(kbase + sw128(tr, c), p.k8 + row * kF8D + c * 16);
-                    cp_async_16(vbase + sw128(tr, c), p.v8 + row * kF8D + c * 16);
-                }
-                cp_async_arrive_noinc(&full[stage]);
-            }
-            ++ld_it;
-        };
-
         float o[kKSteps][NT][4];
         float m[NT][2], l[NT][2];
 #pragma unroll
@@ -216,24 +298,17 @@ __global__ void __launch_bounds__(kF8Threads, 2)
             for (int mt = 0; mt < kKSteps; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
         }
 
-        const int npro = my_n < kF8Stages ? my_n : kF8Stages;
-        if (alive)
-            for (int j = 0; j < npro; ++j) issue(j);
-
-        for (int j = 0; j < my_n; ++j) {
-            if (!alive) continue;  // after a timeout: no waits, no reads, no new copies
+        for (int t = 0; t < cur.ntiles; ++t) {
             const int stage = cs_it % kF8Stages;
-            const uint32_t parity = (cs_it / kF8Stages) & 1;
-            if (!mbar_wait(&full[stage], parity, p.err)) {
+            if (!mbar_wait_warp(&full[stage], (cs_it / kF8Stages) & 1, p.err)) {
                 alive = false;
-                s_abort = 1;
-                continue;
+                break;
             }
             ++cs_it;
             uint8_t* kt = ring + stage * kF8StageBytes;
             uint8_t* vt = kt + kF8TileBytes;
-            const int tb = k0 + (warp + j * kF8Warps) * kF8Tile;
-            const int valid = min(kF8Tile, k1 - tb);
+            const int tb = cur.k0 + t * kF8Tile;
+            const int valid = min(kF8Tile, cur.k1 - tb);
             if (valid < kF8Tile) {  // zero V rows past the end (stale bytes may decode to NaN)
                 for (int ci = lane; ci < (kF8Tile - valid) * 8; ci += 32) {
                     const int tr = valid + (ci >> 3);
@@ -261,6 +336,12 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                     for (int nt = 0; nt < NT; ++nt) mma_f16(sc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
                 }
             }
+            // V fragments of this tile: keys 2c, 2c+1, 8+2c, 9+2c; dims [16 r8, 16 r8 + 16)
+            const uint4 w0 = lds128(vb + sw128(2 * c4, r8));
+            const uint4 w1 = lds128(vb + sw128(2 * c4 + 1, r8));
+            const uint4 w2 = lds128(vb + sw128(8 + 2 * c4, r8));
+            const uint4 w3 = lds128(vb + sw128(9 + 2 * c4, r8));
+
             // mask keys past the end, scale into log2 domain (k_scale folded in)
             const bool v0 = r8 < valid, v1 = r8 + 8 < valid;
             uint32_t pb[NT][2];
@@ -285,22 +366,20 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                     pr[hc + 2] = fast_exp2(x[hc + 2] - mn);
                     l[nt][hc] = l[nt][hc] * alpha[hc] + pr[hc] + pr[hc + 2];
                 }
+                if (alpha[0] != 1.f || alpha[1] != 1.f) {  // the running max moved: rescale O
 #pragma unroll
-                for (int mt = 0; mt < kKSteps; ++mt) {
-                    o[mt][nt][0] *= alpha[0];
-                    o[mt][nt][1] *= alpha[1];
-                    o[mt][nt][2] *= alpha[0];
-                    o[mt][nt][3] *= alpha[1];
+                    for (int mt = 0; mt < kKSteps; ++mt) {
+                        o[mt][nt][0] *= alpha[0];
+                        o[mt][nt][1] *= alpha[1];
+                        o[mt][nt][2] *= alpha[0];
+                        o[mt][nt][3] *= alpha[1];
+                    }
                 }
                 pb[nt][0] = movmatrix_t(pack_f16(pr[0], pr[1]));  // keys 0-7
                 pb[nt][1] = movmatrix_t(pack_f16(pr[2], pr[3]));  // keys 8-15
             }
-            // O^T += V^T . P^T: keys 2c, 2c+1, 8+2c, 9+2c; dims [16 r8, 16 r8 + 16)
+            // O^T += V^T . P^T
             {
-                const uint4 w0 = lds128(vb + sw128(2 * c4, r8));
-                const uint4 w1 = lds128(vb + sw128(2 * c4 + 1, r8));
-                const uint4 w2 = lds128(vb + sw128(8 + 2 * c4, r8));
-                const uint4 w3 = lds128(vb + sw128(9 + 2 * c4, r8));
                 const uint32_t k0w[4] = {w0.x, w0.y, w0.z, w0.w}, k1w[4] = {w1.x, w1.y, w1.z, w1.w};
                 const uint32_t k2w[4] = {w2.x, w2.y, w2.z, w2.w}, k3w[4] = {w3.x, w3.y, w3.z, w3.w};
 #pragma unroll
@@ -323,81 +402,60 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                     }
                 }
             }
+            // every lane's reads of the stage are in registers and used: refill it
             __syncwarp();
-            if (j + kF8Stages < my_n) issue(j + kF8Stages);
+            issue_next();
         }
+        if (!alive) break;
 
-        // ---- merge the warps' partials in smem (the ring is idle now)
-        __syncthreads();
-        constexpr int kH = NT * 8;
-        float* cm = reinterpret_cast<float*>(smem);  // [warps][kH]
-        float* cl = cm + kF8Warps * kH;              // [warps][kH]
-        float* co = cl + kF8Warps * kH;              // [warps][kH][D]
+        // ---- the unit's result straight from registers: O / l (times v_scale)
+        // per head, bf16 to out when the request has one split, else fp32 partials
+        const bool direct = p.nsplit[r] == 1;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
-                float lt = l[nt][hc];
-                lt += __shfl_xor_sync(0xffffffffu, lt, 4);
-                lt += __shfl_xor_sync(0xffffffffu, lt, 8);
-                lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+                float lt_ = l[nt][hc];
+                lt_ += __shfl_xor_sync(0xffffffffu, lt_, 4);
+                lt_ += __shfl_xor_sync(0xffffffffu, lt_, 8);
+                lt_ += __shfl_xor_sync(0xffffffffu, lt_, 16);
                 const int hh = nt * 8 + c4 * 2 + hc;
-                if (lane < 4) {
-                    cm[warp * kH + hh] = m[nt][hc];
-                    cl[warp * kH + hh] = lt;
+                if (hh >= p.G) continue;
+                const int h = g * p.G + hh;
+                const float inv = p.v_scale / lt_;  // the value codes' scale comes out of the sum
+                const float lse_nat = (m[nt][hc] + __log2f(lt_)) * 0.69314718055994531f;
+                // m-tile 2pp row r8 = dim 16 r8 + 4pp, row r8 + 8 = +1; m-tile 2pp+1: +2, +3
+                if (direct) {
+                    __nv_bfloat16* dst = p.out + ((int64_t)r * p.Hq + h) * kF8D + 16 * r8;
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp)
+                        *reinterpret_cast<uint2*>(dst + 4 * pp) =
+                            make_uint2(pack_bf16(o[2 * pp][nt][hc] * inv, o[2 * pp][nt][hc + 2] * inv),
+                                       pack_bf16(o[2 * pp + 1][nt][hc] * inv, o[2 * pp + 1][nt][hc + 2] * inv));
+                    if (p.lse && r8 == 0) p.lse[(int64_t)r * p.Hq + h] = lse_nat;
+                } else {
+                    const int64_t row = (int64_t)cur.pair * p.Hq + h;
+                    float* dst = p.part_o + row * kF8D + 16 * r8;
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp)
+                        *reinterpret_cast<float4*>(dst + 4 * pp) =
+                            make_float4(o[2 * pp][nt][hc] * inv, o[2 * pp][nt][hc + 2] * inv,
+                                        o[2 * pp + 1][nt][hc] * inv, o[2 * pp + 1][nt][hc + 2] * inv);
+                    if (r8 == 0) p.part_lse[row] = lse_nat;
                 }
-#pragma unroll
-                for (int mt = 0; mt < kKSteps; ++mt) {
-                    // m-tile 2p row r8 = dim 16 r8 + 4p, row r8 + 8 = +1; m-tile 2p+1: +2, +3
-                    const int dim = 16 * r8 + 4 * (mt >> 1) + 2 * (mt & 1);
-                    co[(warp * kH + hh) * kF8D + dim] = o[mt][nt][hc];
-                    co[(warp * kH + hh) * kF8D + dim + 1] = o[mt][nt][hc + 2];
-                }
             }
-        __syncthreads();
-        const bool direct = p.nsplit[r] == 1;
-        for (int it = threadIdx.x; it < p.G * (kF8D / 4); it += kF8Threads) {
-            const int hh = it / (kF8D / 4), cc = (it % (kF8D / 4)) * 4;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kF8Warps; ++w) M = fmaxf(M, cm[w * kH + hh]);
-            float Ls = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < kF8Warps; ++w) {
-                const float mw = cm[w * kH + hh];
-                const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-                Ls += wt * cl[w * kH + hh];
-                const float4 x = *reinterpret_cast<const float4*>(co + (w * kH + hh) * kF8D + cc);
-                acc.x += wt * x.x;
-                acc.y += wt * x.y;
-                acc.z += wt * x.z;
-                acc.w += wt * x.w;
-            }
-            const float inv = p.v_scale / Ls;  // the value codes' scale comes out of the sum
-            const float lse_nat = (M + __log2f(Ls)) * 0.69314718055994531f;
-            const int h = g * p.G + hh;
-            if (direct) {
-                uint2 v;
-                v.x = pack_bf16(acc.x * inv, acc.y * inv);
-                v.y = pack_bf16(acc.z * inv, acc.w * inv);
-                *reinterpret_cast<uint2*>(p.out + ((int64_t)r * p.Hq + h) * kF8D + cc) = v;
-                if (p.lse && cc == 0) p.lse[(int64_t)r * p.Hq + h] = lse_nat;
-            } else {
-                const int64_t row = (int64_t)pair * p.Hq + h;
-                *reinterpret_cast<float4*>(p.part_o + row * kF8D + cc) =
-                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                if (cc == 0) p.part_lse[row] = lse_nat;
-            }
-        }
-        // next unit's TMA writes land after these generic smem accesses
-        __syncthreads();
+        // next unit: the one already being loaded; look one further ahead
+        // (every tile of the old unit was issued; the cursor is in nxt, or at
+        // the old unit's end if it has not stepped over yet: then at nxt's start)
+        cur = nxt;
+        if (lw == 0) lt = 0;
+        lw = 0;
+        nxt = cur.unit >= 0 ? fetch() : cur;
     }
-    // A warp that gave up may still have copies in flight; wait (bounded)
-    // for every tile it issued and never consumed, so none outlives the CTA.
+    // No copy may outlive the CTA: wait (bounded) for every tile issued and
+    // never consumed (after a timeout, or loads of units nobody ran).
     while (cs_it < ld_it) {
-        const int stage = cs_it % kF8Stages;
-        mbar_wait(&full[stage], (cs_it / kF8Stages) & 1, p.err);
+        mbar_wait_warp(&full[cs_it % kF8Stages], (cs_it / kF8Stages) & 1, p.err);
         ++cs_it;
     }
 }
@@ -406,6 +464,7 @@ template <int NT, bool kTma>
 static cudaError_t launch_fp8(const CUtensorMap& km, const CUtensorMap& vm, const DecodeGqaParams& p, int num_sms,
                               cudaStream_t stream) {
     auto kern = decode_gqa_fp8_kernel<NT, kTma>;
+    constexpr int kF8Smem = F8Cfg<NT>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;

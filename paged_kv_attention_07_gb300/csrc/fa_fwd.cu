@@ -54,20 +54,29 @@ constexpr int BM = kFaBlockM;  // 128 query rows per query tile
 constexpr int BN = kFaBlockN;  // 128 keys per tile
 static_assert(BM == 128 && BN == 128 && kFaItemTiles == 2, "tile shape is fixed by the TMEM lane count");
 
-template <int D>
+// D: q/k head dim; DV: value head dim (192 / 128 for the pages' non-absorbed
+// MLA prefill, where K carries the 64 rope dims V does not).
+template <int D, int DV>
 struct FaCfg {
-    static constexpr int kChunks = D / 64;                // 64-wide swizzle chunks per row
-    static constexpr int kChunkBytes = 128 * 128;         // 128 rows x 128 B
+    static constexpr int kChunks = D / 64;                 // 64-wide swizzle chunks per q/k row
+    static constexpr int kVChunks = DV / 64;               // ... per v row
+    static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 128 B
     static constexpr int kQBytes = kChunks * kChunkBytes;  // one query tile
-    static constexpr int kKVBytes = kChunks * kChunkBytes;  // one K or V tile
-    static constexpr int kOffQ = 0;                        // the unit's two query tiles
+    static constexpr int kKBytes = kChunks * kChunkBytes;  // one K tile
+    static constexpr int kVBytes = kVChunks * kChunkBytes;  // one V tile
+    // V ring depth: two stages, or one where two would not fit next to the
+    // two query tiles and the two K stages (D = 192: 96 + 96 + 32 KB)
+    static constexpr int kVStages = (2 * kQBytes + 2 * kKBytes + 2 * kVBytes + 1280 <= 232448) ? 2 : 1;
+    static constexpr int kOffQ = 0;                         // the unit's two query tiles
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
-    static constexpr int kOffV = kOffK + 2 * kKVBytes;
-    static constexpr int kOffBar = kOffV + 2 * kKVBytes;
+    static constexpr int kOffV = kOffK + 2 * kKBytes;
+    static constexpr int kOffBar = kOffV + kVStages * kVBytes;
     static constexpr int kSmem = kOffBar + 256 + 1024;
+    static_assert(kSmem <= 232448, "shared memory");
     // TMEM columns: S0, S1 (fp32 128 each; P_k overwrites the first 64 columns
-    // of S_k as bf16 pairs), O0, O1 (fp32 D each)
+    // of S_k as bf16 pairs), O0, O1 (fp32 DV each)
     static constexpr uint32_t kColS = 0, kColO = 256, kTmemCols = 512;
+    static_assert(kColO + 2 * DV <= kTmemCols, "tensor memory");
 };
 
 struct FaUnit {
@@ -120,9 +129,9 @@ PKA_DEVICE int tile_block_id(const FaParams& p, const int32_t* bt, int kb, int c
     return blk;
 }
 
-template <int D>
+template <int D, int DV>
 __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_constant__ FaMaps maps, const FaParams p) {
-    using C = FaCfg<D>;
+    using C = FaCfg<D, DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -214,9 +223,12 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             const bool paged_tma = U.slot != 0 && ctx_tma;
             int blk_next = paged_tma ? tile_block_id(p, bt, U.kb0, U.c1, lane) : 0;
             bool ok = true;
+            const int nstage = which ? C::kVStages : 2;
+            const int nchunk = which ? C::kVChunks : C::kChunks;
+            const int width = which ? DV : D;  // elements per row
             for (int t = 0; t < U.nkv && ok; ++t, ++kv_it) {
-                const int st = kv_it & 1;
-                const uint32_t n = kv_it >> 1;
+                const int st = (int)(kv_it % nstage);
+                const uint32_t n = kv_it / nstage;
                 const int kb = U.kb0 + t * BN;
                 const int blk_mine = blk_next;  // block ids of this tile, one per lane
                 if (paged_tma && t + 1 < U.nkv) blk_next = tile_block_id(p, bt, kb + BN, U.c1, lane);
@@ -227,11 +239,11 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     ok = false;
                     continue;
                 }
-                uint8_t* dst = smem + (which ? C::kOffV : C::kOffK) + st * C::kKVBytes;
+                uint8_t* dst = smem + (which ? C::kOffV + st * C::kVBytes : C::kOffK + st * C::kKBytes);
                 if (U.slot == 0) {
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(full, C::kKVBytes);
-                        for (int c = 0; c < C::kChunks; ++c)
+                        mbar_arrive_expect_tx(full, (uint32_t)(nchunk * C::kChunkBytes));
+                        for (int c = 0; c < nchunk; ++c)
                             tma_load_3d(dst + c * C::kChunkBytes, which ? &maps.vnew : &maps.knew, full, c * 64, U.g,
                                         U.q0 + kb, pol_kv);
                     }
@@ -239,11 +251,11 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     // one lane per block issues that block's boxes (in parallel)
                     const int bs = p.bs;
                     const int nvalid = min(BN / bs, (U.c1 - kb + bs - 1) / bs);
-                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nvalid * C::kChunks * bs * 128));
+                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nvalid * nchunk * bs * 128));
                     __syncwarp();
                     if (lane < nvalid) {
                         const int row = (blk_mine * p.Hkv + U.g) * bs;
-                        for (int c = 0; c < C::kChunks; ++c)
+                        for (int c = 0; c < nchunk; ++c)
                             tma_load_2d(dst + c * C::kChunkBytes + lane * bs * 128, which ? &maps.vc : &maps.kc, full,
                                         c * 64, row, pol_kv);
                     }
@@ -251,8 +263,8 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                     // small blocks: 16-byte copies, rows past the chunk end zero-filled
                     const uint32_t dbase = smem_u32(dst);
                     const __nv_bfloat16* src_base = which ? p.v_cache : p.k_cache;
-                    for (int ci = lane; ci < BN * (D / 8); ci += 32) {
-                        const int row = ci / (D / 8), c = ci % (D / 8);
+                    for (int ci = lane; ci < BN * (width / 8); ci += 32) {
+                        const int row = ci / (width / 8), c = ci % (width / 8);
                         const int pos = kb + row;
                         const bool valid = pos < U.c1;
                         int blk = valid ? __ldg(bt + pos / p.bs) : 0;
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                         }
                         const int64_t grow = ((int64_t)blk * p.Hkv + U.g) * p.bs + (valid ? pos % p.bs : 0);
                         cp_async_16_zfill(dbase + (c >> 3) * C::kChunkBytes + sw128(row, c & 7),
-                                          src_base + grow * D + c * 8, valid);
+                                          src_base + grow * width + c * 8, valid);
                     }
                     asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(full)) : "memory");
                     __syncwarp();
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             if (!ok) break;
         }
         // no copy may outlive the CTA: wait (bounded) for the last one per stage
-        for (int st = 0; st < 2; ++st)
+        for (int st = 0; st < (which ? C::kVStages : 2); ++st)
             if (last[st]) mbar_wait_warp(which ? &v_full[st] : &k_full[st], (last[st] - 1) & 1, p.err);
         if (which == 1 && q_it > 0) mbar_wait_warp(q_full, (q_it - 1) & 1, p.err);
     } else if (warp == 1 || warp == 3) {
@@ -311,7 +323,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                             const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
                             umma_bf16(tbase + C::kColS + k * 128,
                                       umma_desc_sw128(q_s + k * C::kQBytes + off, 16, 1024),
-                                      umma_desc_sw128(k_s + st * C::kKVBytes + off, 16, 1024), idesc_qk,
+                                      umma_desc_sw128(k_s + st * C::kKBytes + off, 16, 1024), idesc_qk,
                                       ks > 0 ? 1u : 0u);
                         }
                         umma_commit(&s_full[k]);
@@ -330,7 +342,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             for (int k = 0; k < 2; ++k)
                 if (nq[k] > 0) mbar_wait(&s_full[k], (nq[k] - 1) & 1, p.err);
         } else if (lane == 0 && warp == 3) {
-            constexpr uint32_t idesc_pv = umma_idesc_bf16(128, D, 0, 1);
+            constexpr uint32_t idesc_pv = umma_idesc_bf16(128, DV, 0, 1);
             const uint32_t v_s = sm_base + C::kOffV;
             uint32_t kv_it = 0;
             uint32_t np[2] = {0, 0};  // products issued from P_k
@@ -341,8 +353,8 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 const FaUnit U = Un;
                 if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
                 for (int t = 0; t < U.nkv; ++t, ++kv_it) {
-                    const int vs = kv_it & 1;
-                    if (!mbar_wait(&v_full[vs], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                    const int vs = (int)(kv_it % C::kVStages);
+                    if (!mbar_wait(&v_full[vs], (kv_it / C::kVStages) & 1, p.err)) { ok = false; break; }
                     for (int k = 0; k < 2; ++k) {
                         if (t >= U.ntk[k]) continue;
                         if (k == 1 && !wait_counter(s_qk0_next, (int)kv_it + 1, p.err)) { ok = false; break; }
@@ -361,8 +373,8 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                             for (int kq = 0; kq < BN / 32; ++kq) {
                                 const int kk = hh * (BN / 32) + kq;
                                 const uint64_t bdesc =
-                                    umma_desc_sw128(v_s + vs * C::kKVBytes + kk * 2048, C::kChunkBytes, 1024);
-                                umma_bf16_ts(tbase + C::kColO + k * D, tbase + C::kColS + k * 128 + kk * 8, bdesc,
+                                    umma_desc_sw128(v_s + vs * C::kVBytes + kk * 2048, C::kChunkBytes, 1024);
+                                umma_bf16_ts(tbase + C::kColO + k * DV, tbase + C::kColS + k * 128 + kk * 8, bdesc,
                                              idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
                             }
                         }
@@ -388,7 +400,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const int wg_tid = threadIdx.x - 128 * (k + 1);
         const uint32_t tS = tbase + lane_off + C::kColS + k * 128;
-        const uint32_t tO = tbase + lane_off + C::kColO + k * D;
+        const uint32_t tO = tbase + lane_off + C::kColO + k * DV;
         const float sl2 = p.scale_log2;
         uint32_t n_s = 0;  // S tiles of this warpgroup (all units)
         uint32_t kv_it = 0;
@@ -550,7 +562,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 // stays 1 for the others)
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                    for (int c = 0; c < D / 16; ++c) {
+                    for (int c = 0; c < DV / 16; ++c) {
                         uint32_t r[16];
                         tmem_ld16(tO + c * 16, r);
                         tmem_wait_ld();
@@ -566,11 +578,11 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 // warpgroup 1's product of the same tile is issued after 0's.
                 if (k == 0 && U.slot != 0 && kb + BN > U.c1) {
                     const uint32_t vi = kv_base + t;
-                    if (!mbar_wait_warp(&v_full[vi & 1], (vi >> 1) & 1, p.err)) { ok = false; break; }
+                    if (!mbar_wait_warp(&v_full[vi % C::kVStages], (vi / C::kVStages) & 1, p.err)) { ok = false; break; }
                     const int valid = U.c1 - kb;
-                    uint8_t* vt = smem + C::kOffV + (vi & 1) * C::kKVBytes;
-                    for (int ci = wg_tid; ci < (BN - valid) * (D / 8); ci += 128) {
-                        const int vr = valid + ci / (D / 8), c = ci % (D / 8);
+                    uint8_t* vt = smem + C::kOffV + (vi % C::kVStages) * C::kVBytes;
+                    for (int ci = wg_tid; ci < (BN - valid) * (DV / 8); ci += 128) {
+                        const int vr = valid + ci / (DV / 8), c = ci % (DV / 8);
                         *reinterpret_cast<uint4*>(vt + (c >> 3) * C::kChunkBytes + sw128(vr, c & 7)) =
                             make_uint4(0, 0, 0, 0);
                     }
@@ -603,14 +615,14 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             // 64 columns per TMEM round trip; each thread writes its own row,
             // 32 bytes (one whole sector) per store where the output allows
 #pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < DV / 64; ++c) {
                 uint32_t r[64];
                 tmem_ld32(tO + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
                 tmem_ld32(tO + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
                 tmem_wait_ld();
                 if (write) {
                     if (final_out) {
-                        __nv_bfloat16* dst = p.out + orow * D + c * 64;
+                        __nv_bfloat16* dst = p.out + orow * DV + c * 64;
                         uint32_t pk[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -627,7 +639,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                                     make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                         }
                     } else {
-                        float* dst = p.ext_o + orow * D + c * 64;  // workspace: 256-byte aligned rows
+                        float* dst = p.ext_o + orow * DV + c * 64;  // workspace: 256-byte aligned rows
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             st_global_v8(dst + j * 8, __float_as_uint(__uint_as_float(r[8 * j]) * inv),
@@ -662,19 +674,21 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
     }
 }
 
-template <int D>
+template <int D, int DV>
 static cudaError_t launch_fa_d(const FaMaps& maps, const FaParams& p, int num_sms, cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D>;
-    const int smem = FaCfg<D>::kSmem;
+    auto kern = fa_fwd_kernel<D, DV>;
+    const int smem = FaCfg<D, DV>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<num_sms, kFaThreads, smem, stream>>>(maps, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_fa_fwd(const FaMaps& maps, const FaParams& p, int head_dim, int num_sms, cudaStream_t stream) {
-    if (head_dim == 128) return launch_fa_d<128>(maps, p, num_sms, stream);
-    if (head_dim == 64) return launch_fa_d<64>(maps, p, num_sms, stream);
+cudaError_t launch_fa_fwd(const FaMaps& maps, const FaParams& p, int head_dim, int head_dim_v, int num_sms,
+                          cudaStream_t stream) {
+    if (head_dim == 128 && head_dim_v == 128) return launch_fa_d<128, 128>(maps, p, num_sms, stream);
+    if (head_dim == 64 && head_dim_v == 64) return launch_fa_d<64, 64>(maps, p, num_sms, stream);
+    if (head_dim == 192 && head_dim_v == 128) return launch_fa_d<192, 128>(maps, p, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 

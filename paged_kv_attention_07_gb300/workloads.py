@@ -246,6 +246,21 @@ def spec_mla_decode(seed: int = 4, num_reqs: int = 64, lo: int = 1024, hi: int =
                      scale=1.0 / math.sqrt(192), mla=True)
 
 
+def spec_mla_prefill(seed: int = 5, n_ext: int = 8, n_pre: int = 4, ext_lo: int = 32768, ext_hi: int = 102400,
+                     ext_new: int = 512, pre_len: int = 2048, heads: int = 128, chunk: int = 32768,
+                     block_size: int = 16) -> BatchSpec:
+    """MLA's non-absorbed prefill/extend (the decompressed form): 8 extends
+    (ctx 32K-100K, 512 new) and 4 prefills of 2048 like the mixed workload,
+    128 heads each with its own K (192 = 128 + 64 rope dims) and V (128),
+    32K-token context chunks, scale 1/sqrt(192)."""
+    rng = np.random.default_rng(seed)
+    ectx = rng.integers(ext_lo, ext_hi, n_ext, endpoint=True).tolist()
+    return BatchSpec(name="mla_prefill_extend", seed=seed, ctx=ectx + [0] * n_pre,
+                     qlen=[ext_new] * n_ext + [pre_len] * n_pre, num_decodes=0, num_extends=n_ext,
+                     num_prefills=n_pre, num_q_heads=heads, num_kv_heads=heads, head_dim=192, head_dim_v=128,
+                     block_size=block_size, scale=1.0 / math.sqrt(192), context_chunk=chunk)
+
+
 def spec_custom(name, ctx, qlen, num_decodes, num_extends, num_prefills, Hq, Hkv, d, dv, bs,
                 scale=None, chunk=32768, num_blocks=0, mla=False, seed=0) -> BatchSpec:
     return BatchSpec(name=name, seed=seed, ctx=list(ctx), qlen=list(qlen), num_decodes=num_decodes,
@@ -274,4 +289,5 @@ ALL_SPECS = {
     "prefill_varlen": spec_prefill,
     "mixed": spec_mixed,
     "mla_decode": spec_mla_decode,
+    "mla_prefill_extend": spec_mla_prefill,
 }

@@ -344,3 +344,48 @@ def test_unified_routing_mostly_one_token_requests():
     assert db.error_word() == 0
     assert db.canaries_intact()
     compare(batch, db.out.float().cpu().numpy().reshape(-1, spec.head_dim_v), db.lse.cpu().numpy().reshape(-1))
+
+
+# ---------------------------------------------------------------- MLA non-absorbed prefill / extend
+# The pages' non-absorbed recipe for MLA prefill and extend runs ordinary
+# attention over the decompressed K (192 dims: 128 + 64 rope) and V (128).
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_nonabsorbed_prefill(G):
+    lens = [1, 2, 63, 64, 65, 130, 300]
+    spec = W.spec_custom("na_pre", ctx=[0] * len(lens), qlen=lens, num_decodes=0, num_extends=0,
+                         num_prefills=len(lens), Hq=2 * G, Hkv=2, d=192, dv=128, bs=16, seed=300 + G)
+    check_batch(W.make_batch(spec))
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 1000])
+@pytest.mark.parametrize("bs", [1, 16, 64])
+def test_nonabsorbed_extend_chunks(chunk, bs):
+    spec = W.spec_custom("na_ext", ctx=[1, 5, 100, 300], qlen=[2, 17, 64, 129], num_decodes=0, num_extends=4,
+                         num_prefills=0, Hq=4, Hkv=4, d=192, dv=128, bs=bs, chunk=chunk, seed=310 + chunk + bs)
+    check_batch(W.make_batch(spec))
+
+
+def test_nonabsorbed_mixed():
+    """Extends (one-token ones included: decodes routed through the extend
+    path) and prefills in one batch."""
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    spec = W.spec_custom("na_mixed", ctx=[700, 3, 40, 2000, 0, 0], qlen=[1, 1, 33, 300, 100, 7], num_decodes=2,
+                         num_extends=2, num_prefills=2, Hq=8, Hkv=8, d=192, dv=128, bs=16, chunk=512, seed=320)
+    batch = W.make_batch(spec)
+    db = DeviceBatch(batch, unified=True)
+    db.step()
+    import torch
+    torch.cuda.synchronize()
+    assert db.error_word() == 0 and db.canaries_intact()
+    compare(batch, db.out.float().cpu().numpy().reshape(-1, 128), db.lse.cpu().numpy().reshape(-1))
+
+
+def test_nonabsorbed_rejects_the_decode_slice():
+    from paged_kv_attention_07_gb300 import pka
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    spec = W.spec_custom("na_dec", ctx=[70, 0], qlen=[1, 5], num_decodes=1, num_extends=0, num_prefills=1,
+                         Hq=4, Hkv=4, d=192, dv=128, bs=16, seed=3)
+    with pytest.raises(RuntimeError):  # the workspace query rejects the shape (no split-KV kernel at d 192)
+        DeviceBatch(W.make_batch(spec))
+    assert pka.pka_workspace_size(1, 0, 1, 6, 4, 4, 192, 128, 5, 71, 32) == 0
