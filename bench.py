@@ -161,17 +161,19 @@ def make_device_batch(spec, device, seed, unified=False, kv_scales=None):
 
 
 def time_steps(db, steps, warmup, flush_bytes=0, kernels=(), barrier=None):
-    """Warm up, then time `steps` steps with CUDA events (L2 flushed between
-    steps when flush_bytes > 0). Returns (ms per step, kernel stats, launches)."""
+    """Warm up, then time `steps` steps with CUDA events on the launching
+    stream (L2 flushed between steps when flush_bytes > 0): that is the step
+    time. Then `steps` more steps with the library's per-launch event timers
+    on, for each kernel's own device time and the launch count (timers between
+    the launches would hold back the overlap of one kernel's launch with its
+    predecessor, so the step time is taken without them).
+    Returns (ms per step, kernel stats, launches per timed pass, (t0, t1))."""
     import torch
     from paged_kv_attention_07_gb300 import pka
     stream = torch.cuda.current_stream()
     flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device=db.device) if flush_bytes else None
     for _ in range(warmup):
         db.step()
-    all_k = list(pka.KERNELS)
-    for k in all_k:
-        pka.pka_kernel_timer(k, True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if barrier:
         barrier()
@@ -188,6 +190,14 @@ def time_steps(db, steps, warmup, flush_bytes=0, kernels=(), barrier=None):
     if barrier:
         barrier()
     ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    all_k = list(pka.KERNELS)
+    for k in all_k:
+        pka.pka_kernel_timer(k, True)
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(float(i))
+        db.step()
+    torch.cuda.synchronize()
     stats, launches = {}, 0
     for k in all_k:
         tot, n, timed = pka.pka_kernel_timer_read(k)

@@ -442,8 +442,7 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
-    cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(PlanHeader), st);
-    if (e != cudaSuccess) return PKA_ERR_CUDA;
+    cudaError_t e = cudaSuccess;  // (the planner clears the header's error word itself)
 
     // ---- plan
     PlanParams pp;

@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pka.h"
 
 #define PKA_DEVICE __device__ __forceinline__
@@ -318,9 +320,41 @@ PKA_DEVICE float fast_exp2(float x) {
     return y;
 }
 
+// ---------------------------------------------------------------- dependent launches
+// The forward pass is a chain of kernels on one stream. Each kernel after the
+// planner is launched as a programmatic dependent (launch_dependent below):
+// it may start while its predecessor still runs, and waits here, before it
+// touches anything, until the predecessor has completed and its writes are
+// visible. Every such kernel calls this first, so each completion implies its
+// predecessors' too.
+PKA_DEVICE void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream start launching (its grid_dep_wait still
+// waits for this whole grid to finish).
+PKA_DEVICE void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Byte offset of 16-byte chunk `c` (0..7) of 128-byte row `row` inside a
 // tile written with the 128-byte swizzle (TMA CU_TENSOR_MAP_SWIZZLE_128B
 // with a 1024-byte aligned base): chunks are XOR-ed with row % 8.
 PKA_DEVICE uint32_t sw128(uint32_t row, uint32_t c) { return row * 128u + ((c ^ (row & 7u)) << 4); }
+
+#ifdef __CUDACC__
+// Launch `kern` as a programmatic dependent of the previous work on `stream`
+// (see grid_dep_wait: the kernel must call it before reading its inputs).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+#endif
 
 }  // namespace pka

@@ -55,6 +55,7 @@ template <int D, int NT, bool kTma>
 __global__ void __launch_bounds__(kDecThreads, 2)
     decode_gqa_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const DecodeGqaParams p) {
+    grid_dep_wait();
     using S = DecGqaSmem<D>;
     constexpr int kSeg = D / 64;
     constexpr int kKSteps = D / 16;
@@ -92,7 +93,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         __syncthreads();
         const int unit = s_unit;
         __syncthreads();
-        if (unit >= num_units) break;
+        if (unit >= num_units) {
+            grid_dep_launch();  // out of work: the split reduction may start launching
+            break;
+        }
         const int pair = unit / p.Hkv, g = unit - pair * p.Hkv;
         const int2 rs = p.pairs[pair];
         const int r = rs.x, split = rs.y;
@@ -356,8 +360,7 @@ static cudaError_t launch_one(const CUtensorMap& km, const CUtensorMap& vm, cons
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    kern<<<num_sms * per_sm, kDecThreads, smem, stream>>>(km, vm, p);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(num_sms * per_sm), dim3(kDecThreads), smem, stream, km, vm, p);
 }
 
 cudaError_t launch_decode_gqa(const CUtensorMap& km, const CUtensorMap& vm, const DecodeGqaParams& p,

@@ -151,6 +151,7 @@ template <int NT, bool kTma>
 __global__ void __launch_bounds__(kF8Threads, F8Cfg<NT>::kMinBlocks)
     decode_gqa_fp8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const DecodeGqaParams p) {
+    grid_dep_wait();
     constexpr int kKSteps = kF8D / 16;
     constexpr int kF8Stages = F8Cfg<NT>::kStages;
     constexpr int kF8RingBytes = F8Cfg<NT>::kRingBytes;
@@ -452,6 +453,7 @@ __global__ void __launch_bounds__(kF8Threads, F8Cfg<NT>::kMinBlocks)
         lw = 0;
         nxt = cur.unit >= 0 ? fetch() : cur;
     }
+    grid_dep_launch();  // out of work: the split reduction may start launching
     // No copy may outlive the CTA: wait (bounded) for every tile issued and
     // never consumed (after a timeout, or loads of units nobody ran).
     while (cs_it < ld_it) {
@@ -471,8 +473,7 @@ static cudaError_t launch_fp8(const CUtensorMap& km, const CUtensorMap& vm, cons
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kF8Threads, kF8Smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    kern<<<num_sms * per_sm, kF8Threads, kF8Smem, stream>>>(km, vm, p);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(num_sms * per_sm), dim3(kF8Threads), kF8Smem, stream, km, vm, p);
 }
 
 cudaError_t launch_decode_gqa_fp8(const CUtensorMap& km, const CUtensorMap& vm, const DecodeGqaParams& p, bool tma,

@@ -43,6 +43,7 @@ PKA_DEVICE uint32_t mla_tile_off(int tr, int c) {  // [9 segs][16 rows][128 B]
 template <int NW, bool kTma>
 __global__ void __launch_bounds__((NW + 1) * 32, 1)
     decode_mla_kernel(const __grid_constant__ CUtensorMap kvmap, const DecodeMlaParams p) {
+    grid_dep_wait();
     using S = MlaSmem<NW>;
     constexpr int HG = NW * 8;  // heads per CTA
     constexpr int kThreads = (NW + 1) * 32;
@@ -277,8 +278,7 @@ static cudaError_t launch_mla(const CUtensorMap& map, const DecodeMlaParams& p, 
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, (NW + 1) * 32, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    kern<<<num_sms * per_sm, (NW + 1) * 32, smem, stream>>>(map, p);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(num_sms * per_sm), dim3((NW + 1) * 32), smem, stream, map, p);
 }
 
 cudaError_t launch_decode_mla(const CUtensorMap& map, const DecodeMlaParams& p, bool tma, int num_sms,

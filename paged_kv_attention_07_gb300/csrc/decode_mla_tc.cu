@@ -83,6 +83,7 @@ PKA_DEVICE bool mla_tc_unit_ok(const DecodeMlaParams& p, const MlaTcUnit& U) {
 __global__ void __launch_bounds__(kMtThreads, 1)
     decode_mla_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap,
                          const DecodeMlaParams p) {
+    grid_dep_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMtOffBar);
@@ -577,8 +578,7 @@ cudaError_t launch_decode_mla_tc(const CUtensorMap& kvmap, const CUtensorMap& qm
                                  int num_sms, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(decode_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMtSmem);
     if (e != cudaSuccess) return e;
-    decode_mla_tc_kernel<<<num_sms, kMtThreads, kMtSmem, stream>>>(kvmap, qmap, p);
-    return cudaGetLastError();
+    return launch_dependent(decode_mla_tc_kernel, dim3(num_sms), dim3(kMtThreads), kMtSmem, stream, kvmap, qmap, p);
 }
 
 }  // namespace pka

@@ -131,6 +131,7 @@ PKA_DEVICE int tile_block_id(const FaParams& p, const int32_t* bt, int kb, int c
 
 template <int D, int DV>
 __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_constant__ FaMaps maps, const FaParams p) {
+    grid_dep_wait();
     using C = FaCfg<D, DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -680,8 +681,7 @@ static cudaError_t launch_fa_d(const FaMaps& maps, const FaParams& p, int num_sm
     const int smem = FaCfg<D, DV>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<num_sms, kFaThreads, smem, stream>>>(maps, p);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(num_sms), dim3(kFaThreads), smem, stream, maps, p);
 }
 
 cudaError_t launch_fa_fwd(const FaMaps& maps, const FaParams& p, int head_dim, int head_dim_v, int num_sms,

@@ -83,15 +83,35 @@ cudaError_t launch_merge_pair(void* out, float* out_lse, const void* a, const fl
 // ------------------------------------------------- multi-way row merge
 // One warp merges n partial rows (row stride `stride` floats between
 // partials) into one bf16 output row and its lse. dv is a multiple of 128.
+// Lane i holds partial i's lse (n <= 32 in one pass); its weight goes to the
+// other lanes by shuffles, and each lane's loads of the n partial pieces are
+// issued back to back, so the merge costs about two memory round trips.
+// w[j] with a runtime j in 0..3, without indexing a register array
+PKA_DEVICE float pick4(const float (&w)[4], int j) {
+    return j == 0 ? w[0] : (j == 1 ? w[1] : (j == 2 ? w[2] : w[3]));
+}
+
 PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int n, int64_t stride_rows,
                                 int dv, __nv_bfloat16* out_row, float* lse_out) {
     const int lane = threadIdx.x & 31;
     float m = -INFINITY;
-    for (int i = lane; i < n; i += 32) m = fmaxf(m, part_lse[(int64_t)i * stride_rows]);
+    float l_mine[4];  // lse of partials lane, lane + 32, ... (n <= 128 kept in registers)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = lane + 32 * j;
+        l_mine[j] = i < n ? part_lse[(int64_t)i * stride_rows] : -INFINITY;
+        m = fmaxf(m, l_mine[j]);
+    }
+    for (int i = lane + 128; i < n; i += 32) m = fmaxf(m, part_lse[(int64_t)i * stride_rows]);
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float wsum = 0.f;
-    for (int i = lane; i < n; i += 32) {
+    float w_mine[4], wsum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w_mine[j] = (m == -INFINITY || l_mine[j] == -INFINITY) ? 0.f : __expf(l_mine[j] - m);
+        wsum += w_mine[j];
+    }
+    for (int i = lane + 128; i < n; i += 32) {
         const float l = part_lse[(int64_t)i * stride_rows];
         wsum += (m == -INFINITY) ? 0.f : __expf(l - m);
     }
@@ -100,10 +120,30 @@ PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int 
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     for (int c = lane * 4; c < dv; c += 128) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < n; ++i) {
-            const float l = part_lse[(int64_t)i * stride_rows];
-            const float w = (m == -INFINITY) ? 0.f : __expf(l - m);
+        int i = 0;
+        for (; i + 4 <= n; i += 4) {  // four partials' loads in flight at once
+            float4 x[4];
+            float w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                x[k] = *reinterpret_cast<const float4*>(part_o + (int64_t)(i + k) * stride_rows * dv + c);
+                const int ii = i + k;
+                const float wl = __shfl_sync(0xffffffffu, pick4(w_mine, (ii >> 5) & 3), ii & 31);
+                w[k] = ii < 128 ? wl
+                                : ((m == -INFINITY) ? 0.f : __expf(part_lse[(int64_t)ii * stride_rows] - m));
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc.x += w[k] * x[k].x;
+                acc.y += w[k] * x[k].y;
+                acc.z += w[k] * x[k].z;
+                acc.w += w[k] * x[k].w;
+            }
+        }
+        for (; i < n; ++i) {
             const float4 x = *reinterpret_cast<const float4*>(part_o + (int64_t)i * stride_rows * dv + c);
+            const float wl = __shfl_sync(0xffffffffu, pick4(w_mine, (i >> 5) & 3), i & 31);
+            const float w = i < 128 ? wl : ((m == -INFINITY) ? 0.f : __expf(part_lse[(int64_t)i * stride_rows] - m));
             acc.x += w * x.x;
             acc.y += w * x.y;
             acc.z += w * x.z;
@@ -121,6 +161,7 @@ PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int 
 // rows (dec_first[r] + s) * Hq + h.
 
 __global__ void __launch_bounds__(256) decode_reduce_kernel(DecodeReduceParams p) {
+    grid_dep_wait();
     if (p.hdr->dec_num_pairs == 0) return;
     const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t total = (int64_t)p.num_decodes * p.Hq;
@@ -139,14 +180,14 @@ cudaError_t launch_decode_reduce(const DecodeReduceParams& p, int num_sms, cudaS
     int64_t blocks = ((int64_t)p.num_decodes * p.Hq + 7) / 8;
     if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
     if (blocks < 1) blocks = 1;
-    decode_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(decode_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p);
 }
 
 // Extend reduction: token i of extend request r has nslot = 1 + chunks
 // partials at rows (ext_base[r] + slot * qlen + i) * Hq + h.
 
 __global__ void __launch_bounds__(256) extend_reduce_kernel(ExtendReduceParams p) {
+    grid_dep_wait();
     if (p.hdr->fa_num_items == 0) return;
     const int nd = p.num_decodes, ne = p.num_extends;
     const int t0 = p.qsl[nd], t1 = p.qsl[nd + ne];
@@ -177,8 +218,7 @@ cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bou
     int64_t blocks = ((int64_t)ext_tokens_bound * p.Hq + 7) / 8;
     if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
     if (blocks < 1) blocks = 1;
-    extend_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(extend_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, p);
 }
 
 }  // namespace pka

@@ -62,15 +62,20 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
     __shared__ int32_t s_hist[kCostBuckets];
     __shared__ int32_t s_err;
     __shared__ unsigned long long s_dec_keys;
+    __shared__ unsigned long long s_wsum[32];
     __shared__ int32_t s_split;
     __shared__ int32_t s_scan[33];
 
+    // the compute kernels are launched as dependents of this one: let them
+    // start (they wait for this grid to finish before reading the plan)
+    grid_dep_launch();
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int nd = p.num_decodes, ne = p.num_extends;
     const int B = nd + ne + p.num_prefills;
     if (tid == 0) {
         s_err = 0;
         s_dec_keys = 0ull;
+        p.hdr->err = 0;  // this call's device error word starts clean
     }
     for (int i = tid; i < kCostBuckets; i += nthr) s_hist[i] = 0;
     __syncthreads();
@@ -99,8 +104,24 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
         }
     }
     if (tid == 0 && p.qsl[B] != p.num_tokens) err |= PKA_DEVERR_QUERY_START_LOC;
-    if (err) atomicOr(&s_err, err);
-    if (dec_keys) atomicAdd(&s_dec_keys, dec_keys);
+    // block-wide OR of the error bits and sum of the decode keys: warp
+    // shuffles, then one pass over the warps' results (no shared atomics on the
+    // 64-bit sum)
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        err |= __shfl_xor_sync(0xffffffffu, err, o);
+        dec_keys += __shfl_xor_sync(0xffffffffu, dec_keys, o);
+    }
+    if ((tid & 31) == 0) {
+        s_wsum[tid >> 5] = dec_keys;
+        if (err) atomicOr(&s_err, err);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long t = 0;
+        for (int w = 0; w < (nthr >> 5); ++w) t += s_wsum[w];
+        s_dec_keys = t;
+    }
     __syncthreads();
 
     if (s_err) {
