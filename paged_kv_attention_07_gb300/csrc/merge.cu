@@ -82,7 +82,7 @@ cudaError_t launch_merge_pair(void* out, float* out_lse, const void* a, const fl
 
 // ------------------------------------------------- multi-way row merge
 // One warp merges n partial rows (row stride `stride` floats between
-// partials) into one bf16 output row and its lse. dv is a multiple of 128.
+// partials) into one bf16 output row and its lse. dv is 64 or a multiple of 128.
 // Lane i holds partial i's lse (n <= 32 in one pass); its weight goes to the
 // other lanes by shuffles, and each lane's loads of the n partial pieces are
 // issued back to back, so the merge costs about two memory round trips.
@@ -118,7 +118,11 @@ PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int 
 #pragma unroll
     for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    for (int c = lane * 4; c < dv; c += 128) {
+    // every lane runs every iteration (the weights come by shuffles); lanes
+    // past dv (dv = 64) only skip their loads and stores
+    for (int c0 = 0; c0 < dv; c0 += 128) {
+        const int c = c0 + lane * 4;
+        const bool active = c < dv;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         int i = 0;
         for (; i + 4 <= n; i += 4) {  // four partials' loads in flight at once
@@ -126,7 +130,8 @@ PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int 
             float w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                x[k] = *reinterpret_cast<const float4*>(part_o + (int64_t)(i + k) * stride_rows * dv + c);
+                x[k] = active ? *reinterpret_cast<const float4*>(part_o + (int64_t)(i + k) * stride_rows * dv + c)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
                 const int ii = i + k;
                 const float wl = __shfl_sync(0xffffffffu, pick4(w_mine, (ii >> 5) & 3), ii & 31);
                 w[k] = ii < 128 ? wl
@@ -141,7 +146,8 @@ PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int 
             }
         }
         for (; i < n; ++i) {
-            const float4 x = *reinterpret_cast<const float4*>(part_o + (int64_t)i * stride_rows * dv + c);
+            const float4 x = active ? *reinterpret_cast<const float4*>(part_o + (int64_t)i * stride_rows * dv + c)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
             const float wl = __shfl_sync(0xffffffffu, pick4(w_mine, (i >> 5) & 3), i & 31);
             const float w = i < 128 ? wl : ((m == -INFINITY) ? 0.f : __expf(part_lse[(int64_t)i * stride_rows] - m));
             acc.x += w * x.x;
@@ -149,10 +155,12 @@ PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int 
             acc.z += w * x.z;
             acc.w += w * x.w;
         }
-        uint2 o;
-        o.x = pack_bf16(acc.x * inv, acc.y * inv);
-        o.y = pack_bf16(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(out_row + c) = o;
+        if (active) {
+            uint2 o;
+            o.x = pack_bf16(acc.x * inv, acc.y * inv);
+            o.y = pack_bf16(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(out_row + c) = o;
+        }
     }
     if (lane == 0 && lse_out) *lse_out = (wsum > 0.f) ? m + __logf(wsum) : -INFINITY;
 }
