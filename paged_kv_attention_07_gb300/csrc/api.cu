@@ -38,8 +38,8 @@ cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bou
 int decode_gqa_target_units(int num_sms);
 int decode_mla_heads_per_cta(int Hq);
 bool decode_mla_tc_supported(int Hq);
-cudaError_t launch_decode_mla_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecodeMlaParams& p,
-                                 int num_sms, cudaStream_t stream);
+cudaError_t launch_decode_mla_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, const CUtensorMap& gmap,
+                                 const DecodeMlaParams& p, int num_sms, cudaStream_t stream);
 
 // MLA decode units per (request, split): on the tensor-core kernel two value
 // halves per group of 128 heads, otherwise one unit per 64-head group.
@@ -484,14 +484,17 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
         const bool tma = block_size >= 8;
         if (is_mla) {
             const bool tc = decode_mla_tc_supported(num_q_heads);
-            CUtensorMap map, qmap;
+            CUtensorMap map, qmap, gmap;
             std::memset(&map, 0, sizeof(map));
             std::memset(&qmap, 0, sizeof(qmap));
+            std::memset(&gmap, 0, sizeof(gmap));
             if (tma && !encode_rows(&map, k_cache, (uint64_t)cache_rows, 576,
                                     (uint32_t)std::min(block_size, tc ? 64 : 16)))
                 return PKA_ERR_CUDA;
             if (tc && !encode_heads(&qmap, q, (uint64_t)num_tokens, (uint64_t)num_q_heads, 576, 128))
                 return PKA_ERR_CUDA;
+            // one-row boxes for the tensor-core kernel's row gathers
+            if (tc && !encode_rows(&gmap, k_cache, (uint64_t)cache_rows, 576, 1)) return PKA_ERR_CUDA;
             DecodeMlaParams dp;
             dp.q = static_cast<const __nv_bfloat16*>(q);
             dp.kv = static_cast<const __nv_bfloat16*>(k_cache);
@@ -511,9 +514,11 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
             dp.Hq = num_q_heads;
             dp.bs = block_size;
             dp.groups = tc ? num_q_heads / 128 : num_q_heads / decode_mla_heads_per_cta(num_q_heads);
+            dp.cache_rows = (int)cache_rows;
             dp.scale_log2 = scale_log2;
             if ((e = timed(PKA_KERNEL_DECODE, st, [&] {
-                     return tc ? launch_decode_mla_tc(map, qmap, dp, sms, st) : launch_decode_mla(map, dp, tma, sms, st);
+                     return tc ? launch_decode_mla_tc(map, qmap, gmap, dp, sms, st)
+                               : launch_decode_mla(map, dp, tma, sms, st);
                  })) != cudaSuccess)
                 return PKA_ERR_CUDA;
         } else {

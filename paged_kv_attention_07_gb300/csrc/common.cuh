@@ -164,6 +164,19 @@ PKA_DEVICE void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* ba
         : "memory");
 }
 
+// Four rows of a 2-D map gathered into consecutive 128-byte rows of shared
+// memory: rows r0..r3 (any order, any rows; an out-of-range row reads the
+// fill value, zeros), columns [c0, c0 + box width). The map's box is one row
+// high (the gather form's requirement).
+PKA_DEVICE void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int r0, int r1, int r2,
+                            int r3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+        : "memory");
+}
+
 // L2 prefetch of a tile (no shared memory, no completion tracking).
 PKA_DEVICE void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

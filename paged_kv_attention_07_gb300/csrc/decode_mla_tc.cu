@@ -21,9 +21,10 @@
 //     [256, 512) O   fp32, this unit's 256 value dims
 // Shared memory: q[:, 320:576] (64 KB, the A operand of the last 16 k-steps)
 // and a 2-stage ring of 64-key latent tiles (72 KB each), loaded with TMA
-// boxes of 64 dims x min(block size, 64) rows walked through the block table
-// (16-byte cp.async copies below block size 8 and for a split's last,
-// partial tile, whose missing rows are zero-filled).
+// boxes of 64 dims x min(block size, 64) rows walked through the block table;
+// below block size 8, and for a split's last, partial tile, TMA gathers of
+// four latent rows x 64 dims each (rows past the split's end are read at an
+// out-of-range row, which TMA fills with zeros).
 //
 // Persistent CTAs, one per SM, allocate tensor memory once and take units
 // from an atomic counter; warp 0 publishes each unit index to the other roles
@@ -82,7 +83,7 @@ PKA_DEVICE bool mla_tc_unit_ok(const DecodeMlaParams& p, const MlaTcUnit& U) {
 
 __global__ void __launch_bounds__(kMtThreads, 1)
     decode_mla_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap,
-                         const DecodeMlaParams p) {
+                         const __grid_constant__ CUtensorMap gmap, const DecodeMlaParams p) {
     grid_dep_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         s_abort = 0;
         tma_prefetch_desc(&kvmap);
         tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&gmap);
     }
     if (warp == 1) tmem_alloc(&s_tmem, kMtCols);
     tc_fence_before();
@@ -220,8 +222,15 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 const int tb = U.k0 + t * kMtTile;
                 const int valid = min(kMtTile, U.k1 - tb);
                 const bool tma = use_tma && valid == kMtTile;
-                const int blk_lo = (!tma && tb + lane < U.k1) ? block_of(tb + lane) : 0;
-                const int blk_hi = (!tma && tb + 32 + lane < U.k1) ? block_of(tb + 32 + lane) : 0;
+                // gather path: lane l < 16 takes rows 4l .. 4l + 3 of the tile
+                int grow[4] = {0, 0, 0, 0};
+                if (!tma && lane < kMtTile / 4) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int pos = tb + 4 * lane + k;
+                        grow[k] = pos < U.k1 ? block_of(pos) * p.bs + (pos % p.bs) : p.cache_rows;  // out of range: zeros
+                    }
+                }
                 // part 0: the score-only chunks, part 1: the value chunks
                 {
                     uint64_t* empty = part ? &kv_empty_v[st] : &kv_empty[st];
@@ -244,43 +253,15 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                                     tma_load_2d(dst + c * kMtChunk + lane * rows * 128, &kvmap, full, c * 64, row, pol);
                         }
                     } else {
-                        // 16-byte copies, the whole warp on one row at a time (512
-                        // contiguous bytes per instruction); the rows' block ids were
-                        // loaded once, two per lane, and are shuffled to the warp.
-                        // Rows past the split's end are zero-filled (no NaN from
-                        // slots the batch does not own).
-                        const uint32_t dbase = smem_u32(dst);
-                        const int npieces = 8 * __popc(cmask);
-                        // this lane's pieces: chunk and 16-byte index within the chunk
-                        int pc[2], pk[2];
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const int pi = lane + 32 * j;
-                            int nth = pi >> 3, c = 0;
-                            for (int cc = 0; cc < 9; ++cc)
-                                if ((cmask >> cc) & 1) {
-                                    if (nth == 0) c = cc;
-                                    --nth;
-                                }
-                            pc[j] = c;
-                            pk[j] = pi & 7;
-                        }
-                        for (int tr = 0; tr < kMtTile; ++tr) {
-                            const int b_lo = __shfl_sync(0xffffffffu, blk_lo, tr & 31);
-                            const int b_hi = __shfl_sync(0xffffffffu, blk_hi, tr & 31);
-                            const int pos = tb + tr;
-                            const bool in = pos < U.k1;
-                            const __nv_bfloat16* src =
-                                p.kv + ((int64_t)(tr < 32 ? b_lo : b_hi) * p.bs + (in ? pos % p.bs : 0)) * kMtD;
-#pragma unroll
-                            for (int j = 0; j < 2; ++j)
-                                if (lane + 32 * j < npieces)
-                                    cp_async_16_zfill(dbase + pc[j] * kMtChunk + sw128(tr, pk[j]),
-                                                      src + pc[j] * 64 + pk[j] * 8, in);
-                        }
-                        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(full)) : "memory");
+                        // TMA gathers, 4 rows x 64 dims per instruction, 16 lanes in
+                        // parallel; every chunk's bytes arrive (rows past the end as zeros)
+                        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(__popc(cmask) * kMtChunk));
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(full);
+                        if (lane < kMtTile / 4)
+                            for (int c = 0; c < 9; ++c)
+                                if ((cmask >> c) & 1)
+                                    tma_gather4(dst + c * kMtChunk + lane * 4 * 128, &gmap, full, c * 64, grow[0], grow[1],
+                                                grow[2], grow[3]);
                     }
                 }
                 if (!ok) break;
@@ -574,11 +555,12 @@ __global__ void __launch_bounds__(kMtThreads, 1)
 
 bool decode_mla_tc_supported(int Hq) { return Hq > 0 && Hq % 128 == 0; }
 
-cudaError_t launch_decode_mla_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecodeMlaParams& p,
-                                 int num_sms, cudaStream_t stream) {
+cudaError_t launch_decode_mla_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, const CUtensorMap& gmap,
+                                 const DecodeMlaParams& p, int num_sms, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(decode_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMtSmem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(decode_mla_tc_kernel, dim3(num_sms), dim3(kMtThreads), kMtSmem, stream, kvmap, qmap, p);
+    return launch_dependent(decode_mla_tc_kernel, dim3(num_sms), dim3(kMtThreads), kMtSmem, stream, kvmap, qmap, gmap,
+                            p);
 }
 
 }  // namespace pka

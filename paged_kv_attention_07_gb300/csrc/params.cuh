@@ -50,6 +50,7 @@ struct DecodeMlaParams {
     float* lse;
     int64_t num_blocks;
     int max_blocks, Hq, bs, groups;  // groups = Hq / (8 * NW)
+    int cache_rows;                  // num_blocks * bs (a row index past the cache)
     float scale_log2;
 };
 
