@@ -259,7 +259,8 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
               ("fa_fwd.cu", "fa_fwd_mla_prefill_extend")),
              ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0,
               ("decode_mla_tc.cu", "decode_mla_tc_mla_decode_bs64")),
-             ("mla_decode_bs1", W.spec_mla_decode(block_size=1), "decode", "hbm", 0, None)]
+             ("mla_decode_bs1", W.spec_mla_decode(block_size=1), "decode", "hbm", 0,
+              ("decode_mla_tc.cu", "decode_mla_tc_mla_decode_bs1"))]
     for name, spec, dom, bound, flush, tkey in cases:
         traffic = kernel_traffic(*tkey) if tkey else None
         fp8 = name.endswith("_fp8")
@@ -466,6 +467,10 @@ def run_ours(args):
 WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "decode_gqa_fp8": W.spec_decode_gqa,
              "prefill_varlen": W.spec_prefill, "mixed": W.spec_mixed,
              "mla_decode_bs64": W.spec_mla_decode, "mla_prefill_extend": W.spec_mla_prefill,
+             # profiling cases: 64 heads (the warp-MMA MLA kernel), and the
+             # non-absorbed prefill/extend at a size an ncu replay handles
+             "mla_decode_h64": lambda: W.spec_mla_decode(heads=64),
+             "mla_prefill_extend_small": lambda: W.spec_mla_prefill(n_ext=2, n_pre=1, heads=32),
              "mla_decode_bs1": lambda: W.spec_mla_decode(block_size=1),
              "mixed_unified": W.spec_mixed, "mixed_unordered": W.spec_mixed}
 

@@ -236,12 +236,12 @@ def spec_mixed(seed: int = 3, n_dec: int = 128, n_ext: int = 8, n_pre: int = 4,
 
 
 def spec_mla_decode(seed: int = 4, num_reqs: int = 64, lo: int = 1024, hi: int = 32768,
-                    block_size: int = 64) -> BatchSpec:
+                    block_size: int = 64, heads: int = 128) -> BatchSpec:
     """Absorbed MLA decode: 128 heads over one 576-dim latent (V = first 512)."""
     rng = np.random.default_rng(seed)
     ctx = rng.integers(lo, hi, num_reqs, endpoint=True).tolist()
     return BatchSpec(name="mla_decode", seed=seed, ctx=ctx, qlen=[1] * num_reqs,
-                     num_decodes=num_reqs, num_extends=0, num_prefills=0, num_q_heads=128,
+                     num_decodes=num_reqs, num_extends=0, num_prefills=0, num_q_heads=heads,
                      num_kv_heads=1, head_dim=576, head_dim_v=512, block_size=block_size,
                      scale=1.0 / math.sqrt(192), mla=True)
 
