@@ -85,3 +85,62 @@ def attention_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, query_star
     out, lse = attention(q, codes_to_bf16_bits(k_codes), codes_to_bf16_bits(v_codes), block_table,
                          query_start_loc, seq_lens, scale * k_scale, block_size, **kw)
     return out * v_scale, lse
+
+
+def _bf16_bits_to_f64(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def step_reference_fp8(q, k_codes, v_codes, k_new, v_new, k_scale, v_scale, block_table, query_start_loc,
+                       seq_lens, num_decodes, scale, block_size):
+    """One step over an 8-bit cache, float64, written out per request and head.
+
+    Which values a query sees (the pages' prefill listing: the new tokens'
+    attention runs on the step's own K/V, the context chunks on the cache
+    gathered and dequantised, `gather_and_maybe_dequant_cache`):
+      * a decode request (the first `num_decodes`) reads every position from
+        the cache, its own new token included (the cache write stored it):
+        K_j = k_scale * code_j, V_j = v_scale * code_j;
+      * an extend or prefill request reads its ctx cached positions from the
+        cache the same way and its new tokens' K/V from k_new / v_new (bf16).
+    Query i of a request with ctx cached tokens sits at position ctx + i and
+    sees keys 0 .. ctx + i (bottom-right causal); s_j = scale * <q, K_j>,
+    lse = log sum_j e^{s_j}, out = sum_j e^{s_j - lse} V_j.
+
+    q, k_new, v_new: bf16 bits [T, H, d]; k_codes / v_codes: uint8
+    [blocks, Hkv, bs, d]. Returns (out [T * Hq, dv], lse [T * Hq]) in the
+    flattened row order t * Hq + h."""
+    qf = _bf16_bits_to_f64(q)
+    kn, vn = _bf16_bits_to_f64(k_new), _bf16_bits_to_f64(v_new)
+    T, Hq, d = qf.shape
+    Hkv, dv = k_codes.shape[1], v_codes.shape[3]
+    G = Hq // Hkv
+    kdec, vdec = dequantize(k_codes, k_scale), dequantize(v_codes, v_scale)
+    out = np.zeros((T, Hq, dv))
+    lse = np.zeros((T, Hq))
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    for r in range(len(seq_lens)):
+        t0, t1 = int(qsl[r]), int(qsl[r + 1])
+        n, s = t1 - t0, int(seq_lens[r])
+        ctx = s - n
+        cached = s if r < num_decodes else ctx  # positions read from the cache
+        pos = np.arange(cached)
+        blk = np.asarray(block_table[r], dtype=np.int64)[pos // block_size]
+        for hk in range(Hkv):
+            K = kdec[blk, hk, pos % block_size]
+            V = vdec[blk, hk, pos % block_size]
+            if cached < s:
+                K = np.concatenate([K, kn[t0:t1, hk]])
+                V = np.concatenate([V, vn[t0:t1, hk]])
+            for g in range(G):
+                h = hk * G + g
+                sc = scale * (qf[t0:t1, h] @ K.T)  # [n, s]
+                visible = np.arange(s)[None, :] <= (ctx + np.arange(n))[:, None]
+                sc = np.where(visible, sc, -np.inf)
+                m = sc.max(axis=1, keepdims=True)
+                e = np.exp(sc - m)
+                den = e.sum(axis=1, keepdims=True)
+                out[t0:t1, h] = (e @ V) / den
+                lse[t0:t1, h] = (m + np.log(den))[:, 0]
+    return out.reshape(T * Hq, dv), lse.reshape(T * Hq)

@@ -128,3 +128,83 @@ def test_float32_quotient_differs_from_exact_only_at_double_rounding():
     a, b = fp8.quantize_f32(x, s), fp8.quantize(x.astype(np.float64), np.float64(np.float32(s)))
     assert (a != b).sum() <= 5
     assert np.all(np.abs(fp8.decode(a) - fp8.decode(b))[a != b] <= 2.0 ** -3 * np.abs(fp8.decode(b))[a != b] + 2 ** -9)
+
+
+def _snap_batch(batch, s):
+    """The batch with its context rows and its decodes' new rows moved onto
+    the grid of E4M3 values x s (s a power of two: those values are bf16
+    values, so a cache of their codes holds them exactly); the extends' and
+    prefills' new rows stay arbitrary bf16."""
+    from paged_kv_attention_07_gb300 import workloads as W
+    spec = batch.spec
+    snap_rows = [batch.ctx_index]
+    for r in range(spec.num_decodes):
+        snap_rows.append(batch.seq_start[r] + np.arange(spec.ctx[r], spec.ctx[r] + spec.qlen[r]))
+    idx = np.concatenate(snap_rows)
+    for name in ("k_seq", "v_seq"):
+        a = getattr(batch, name).copy()
+        x = W.bf16_bits_to_f32(a[idx]).astype(np.float64)
+        a[idx] = W.to_bf16_bits(fp8.dequantize(fp8.quantize(x, s), s).astype(np.float32))
+        setattr(batch, name, a)
+    return batch
+
+
+def _codes_cache(batch, s):
+    """Codes of every position (what the 8-bit cache write leaves), NaN code elsewhere."""
+    from paged_kv_attention_07_gb300 import workloads as W
+    spec = batch.spec
+    shape = (batch.num_blocks, spec.num_kv_heads, spec.block_size)
+    kc = np.full(shape + (spec.head_dim,), 0x7F, np.uint8)
+    vc = np.full(shape + (spec.head_dim_v,), 0x7F, np.uint8)
+    blk, off = batch.slot_all // spec.block_size, batch.slot_all % spec.block_size
+    for cache, seq in ((kc, batch.k_seq), (vc, batch.v_seq)):
+        codes = fp8.quantize_f32(W.bf16_bits_to_f32(seq), s)
+        for hk in range(spec.num_kv_heads):
+            cache[blk, hk, off] = codes[:, hk]
+    return kc, vc
+
+
+@pytest.mark.parametrize("bs,seed", [(8, 21), (1, 22), (16, 23)])
+def test_step_reference_fp8_equals_plain_attention_on_exact_codes(bs, seed):
+    """When every cached value is exactly a code's value, the 8-bit step
+    reference must equal the plain definition (the C oracle) on a bf16 cache
+    holding the same values, with the extends' and prefills' new tokens taken
+    at full bf16 precision (they are not on the E4M3 grid here, so reading
+    them from the cache instead would fail this)."""
+    import oracle
+    from paged_kv_attention_07_gb300 import workloads as W
+    s = 2.0 ** -3
+    spec = W.spec_custom("f8step", ctx=[5, 33, 20, 47, 0, 0], qlen=[1, 1, 7, 18, 9, 3], num_decodes=2,
+                         num_extends=2, num_prefills=2, Hq=6, Hkv=2, d=16, dv=8, bs=bs, seed=seed)
+    batch = _snap_batch(W.make_batch(spec), s)
+    new_ext = batch.k_seq[batch.new_index][2:]  # the extends' and prefills' new rows
+    x = W.bf16_bits_to_f32(new_ext).astype(np.float64)
+    assert np.any(fp8.dequantize(fp8.quantize(x, s), s) != x)  # off the grid
+    kc, vc = _codes_cache(batch, s)
+    out, lse = fp8.step_reference_fp8(batch.q, kc, vc, batch.k_new, batch.v_new, s, s, batch.block_table,
+                                      batch.query_start_loc, batch.seq_lens, spec.num_decodes, spec.scale,
+                                      spec.block_size)
+    kb, vb = oracle.populate_cache(batch, "all")
+    ref_o, ref_l = oracle.attention(batch.q, kb, vb, batch.block_table, batch.query_start_loc, batch.seq_lens,
+                                    spec.scale, spec.block_size, head_dim_v=spec.head_dim_v)
+    np.testing.assert_allclose(out, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l, rtol=0, atol=1e-12)
+
+
+def test_step_reference_fp8_decodes_read_their_own_token_from_the_cache():
+    """A decode-only step: every position, the new one included, comes from
+    the codes, so the reference equals the oracle's attention over the 8-bit
+    cache with arbitrary (not power-of-two) scales."""
+    from paged_kv_attention_07_gb300 import workloads as W
+    spec = W.spec_custom("f8dec", ctx=[3, 40, 17], qlen=[1, 1, 1], num_decodes=3, num_extends=0,
+                         num_prefills=0, Hq=4, Hkv=1, d=16, dv=16, bs=4, seed=31)
+    batch = W.make_batch(spec)
+    ks, vs = 0.0137, 0.0211
+    kc = _codes_cache(batch, ks)[0]
+    vc = _codes_cache(batch, vs)[1]
+    out, lse = fp8.step_reference_fp8(batch.q, kc, vc, batch.k_new, batch.v_new, ks, vs, batch.block_table,
+                                      batch.query_start_loc, batch.seq_lens, 3, spec.scale, spec.block_size)
+    ref_o, ref_l = fp8.attention_fp8(batch.q, kc, vc, ks, vs, batch.block_table, batch.query_start_loc,
+                                     batch.seq_lens, spec.scale, spec.block_size)
+    np.testing.assert_allclose(out, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l, rtol=0, atol=1e-12)
