@@ -25,7 +25,6 @@ namespace pka {
 
 namespace {
 
-constexpr int kCwRows = 4;       // rows per warp step
 constexpr int kCwMaxPieces = 4;  // 16-byte pieces per lane per row (K + V <= 128 pieces = 1024 bf16)
 
 struct CacheWriteParams {
@@ -57,41 +56,56 @@ PKA_DEVICE uint2 quantize8(uint4 x, float s) {
     return r;
 }
 
-template <bool kFp8, int kCwPieces>
+// Rows per warp step: enough 16-byte pieces per lane in flight to cover the
+// load latency (one piece per lane per row at d = dv = 128).
+template <int kCwPieces>
+constexpr int cw_rows() {
+    return kCwPieces == 1 ? 8 : 4;
+}
+
+// kWide: 64-bit row and slot arithmetic, only when T * Hkv or the slot count
+// reaches 2^31 (64-bit division by a runtime divisor is a long software
+// sequence; the 32-bit one is a few instructions).
+template <bool kFp8, int kCwPieces, bool kWide>
 __global__ void __launch_bounds__(256) cache_write_kernel(CacheWriteParams p) {
+    using Idx = typename std::conditional<kWide, int64_t, uint32_t>::type;
+    constexpr int kRows = cw_rows<kCwPieces>();
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int64_t rows = p.num_tokens * p.num_kv_heads;
-    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const Idx warp = (Idx)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const Idx rows = (Idx)(p.num_tokens * p.num_kv_heads);
+    const Idx nwarps = (Idx)gridDim.x * (blockDim.x >> 5);
+    const Idx hkv = (Idx)p.num_kv_heads, bs = (Idx)p.block_size;
     const int nv = p.k_vecs + p.v_vecs;
-    for (int64_t r0 = warp * kCwRows; r0 < rows; r0 += nwarps * kCwRows) {
-        int64_t slot[kCwRows];
-        uint4 val[kCwRows][kCwPieces];
+    for (Idx r0 = warp * kRows; r0 < rows; r0 += nwarps * kRows) {
+        int64_t slot[kRows];
+        uint4 val[kRows][kCwPieces];
 #pragma unroll
-        for (int i = 0; i < kCwRows; ++i) {
-            const int64_t row = r0 + i;
+        for (int i = 0; i < kRows; ++i) {
+            const Idx row = r0 + i;
             const bool in = row < rows;
-            slot[i] = in ? __ldg(p.slots + row / p.num_kv_heads) : -1;
+            slot[i] = in ? __ldg(p.slots + row / hkv) : -1;
 #pragma unroll
             for (int j = 0; j < kCwPieces; ++j) {
                 const int c = lane + 32 * j;
                 if (in && c < nv)
-                    val[i][j] = c < p.k_vecs ? __ldcs(p.k + row * p.k_vecs + c) : __ldcs(p.v + row * p.v_vecs + (c - p.k_vecs));
+                    val[i][j] = c < p.k_vecs ? __ldcs(p.k + (int64_t)row * p.k_vecs + c)
+                                             : __ldcs(p.v + (int64_t)row * p.v_vecs + (c - p.k_vecs));
             }
         }
 #pragma unroll
-        for (int i = 0; i < kCwRows; ++i) {
-            const int64_t row = r0 + i;
-            const int64_t s = slot[i];
-            if (row >= rows || s < 0) continue;
-            if (s >= p.num_slots) {
+        for (int i = 0; i < kRows; ++i) {
+            const Idx row = r0 + i;
+            const int64_t s64 = slot[i];
+            if (row >= rows || s64 < 0) continue;
+            if (s64 >= p.num_slots) {
                 if (lane == 0) set_error(p.err, PKA_DEVERR_SLOT);
                 continue;
             }
-            const int64_t t = row / p.num_kv_heads;
-            const int h = (int)(row - t * p.num_kv_heads);
-            const int64_t blk = s / p.block_size;
-            const int64_t dst_row = (blk * p.num_kv_heads + h) * p.block_size + (s - blk * p.block_size);
+            const Idx s = (Idx)s64;  // < num_slots, which fits Idx
+            const Idx t = row / hkv;
+            const Idx h = row - t * hkv;
+            const Idx blk = s / bs;
+            const int64_t dst_row = ((int64_t)blk * hkv + h) * bs + (s - blk * bs);
 #pragma unroll
             for (int j = 0; j < kCwPieces; ++j) {
                 const int c = lane + 32 * j;
@@ -109,6 +123,15 @@ __global__ void __launch_bounds__(256) cache_write_kernel(CacheWriteParams p) {
             }
         }
     }
+}
+
+// Resident CTAs per SM of one instantiation (the grid is sized to one full
+// wave: the grid-stride loop then needs no second, partial wave).
+template <typename K>
+int cw_blocks_per_sm(K kern) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 256, 0) != cudaSuccess || n < 1) n = 1;
+    return n;
 }
 
 }  // namespace
@@ -134,26 +157,33 @@ cudaError_t launch_cache_write(const void* k, const void* v, const int64_t* slot
     const int pieces = (p.k_vecs + p.v_vecs + 31) / 32;  // per lane per row
     if (pieces > kCwMaxPieces) return cudaErrorInvalidValue;
     const int64_t rows = T * Hkv;
-    int64_t blocks = (rows + 8 * kCwRows - 1) / (8 * kCwRows);
-    const int64_t cap = (int64_t)num_sms * 8;  // 8 blocks of 8 warps fill an SM
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    auto go = [&](auto fp8_c, auto pieces_c) {
-        cache_write_kernel<decltype(fp8_c)::value, decltype(pieces_c)::value><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    const bool wide = rows >= ((int64_t)1 << 31) || p.num_slots >= ((int64_t)1 << 31);
+    auto go = [&](auto fp8_c, auto pieces_c, auto wide_c) {
+        constexpr bool F = decltype(fp8_c)::value, W = decltype(wide_c)::value;
+        constexpr int P = decltype(pieces_c)::value;
+        auto kern = cache_write_kernel<F, P, W>;
+        static const int per_sm = cw_blocks_per_sm(kern);  // one value per instantiation
+        const int64_t need = (rows + 8 * cw_rows<P>() - 1) / (8 * cw_rows<P>());
+        int64_t blocks = std::min<int64_t>(need, (int64_t)num_sms * per_sm);
+        if (blocks < 1) blocks = 1;
+        kern<<<(unsigned)blocks, 256, 0, stream>>>(p);
     };
     using T_ = std::true_type;
     using F_ = std::false_type;
     using P1 = std::integral_constant<int, 1>;
     using P2 = std::integral_constant<int, 2>;
     using P4 = std::integral_constant<int, 4>;
+    auto by_pieces = [&](auto fp8_c, auto wide_c) {
+        if (pieces == 1) go(fp8_c, P1{}, wide_c);
+        else if (pieces == 2) go(fp8_c, P2{}, wide_c);
+        else go(fp8_c, P4{}, wide_c);
+    };
     if (fp8) {
-        if (pieces == 1) go(T_{}, P1{});
-        else if (pieces == 2) go(T_{}, P2{});
-        else go(T_{}, P4{});
+        if (wide) by_pieces(T_{}, T_{});
+        else by_pieces(T_{}, F_{});
     } else {
-        if (pieces == 1) go(F_{}, P1{});
-        else if (pieces == 2) go(F_{}, P2{});
-        else go(F_{}, P4{});
+        if (wide) by_pieces(F_{}, T_{});
+        else by_pieces(F_{}, F_{});
     }
     return cudaGetLastError();
 }

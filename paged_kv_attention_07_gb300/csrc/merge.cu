@@ -85,14 +85,70 @@ cudaError_t launch_merge_pair(void* out, float* out_lse, const void* a, const fl
 // partials) into one bf16 output row and its lse. dv is 64 or a multiple of 128.
 // Lane i holds partial i's lse (n <= 32 in one pass); its weight goes to the
 // other lanes by shuffles, and each lane's loads of the n partial pieces are
-// issued back to back, so the merge costs about two memory round trips.
+// issued four at a time, so the merge costs about 1 + n / 4 memory round trips
+// (rows of at most kSmallMerge partials take the one-round-trip path below).
 // w[j] with a runtime j in 0..3, without indexing a register array
 PKA_DEVICE float pick4(const float (&w)[4], int j) {
     return j == 0 ? w[0] : (j == 1 ? w[1] : (j == 2 ? w[2] : w[3]));
 }
 
+// Up to kSmallMerge partials: the LSEs and the first 128-dim chunk of every
+// partial are loaded together before any weight is known, so a row of up to
+// 128 dims costs one memory round trip (plus one per further 128 dims).
+// Summation order is the partials' order, as in the general path.
+constexpr int kSmallMerge = 8;
+
+PKA_DEVICE void merge_rows_warp_small(const float* part_o, const float* part_lse, int n, int64_t stride_rows,
+                                      int dv, __nv_bfloat16* out_row, float* lse_out) {
+    const int lane = threadIdx.x & 31;
+    auto load_chunk = [&](int c0, float4 (&x)[kSmallMerge]) {
+        const int c = c0 + lane * 4;
+#pragma unroll
+        for (int k = 0; k < kSmallMerge; ++k)
+            x[k] = (k < n && c < dv) ? *reinterpret_cast<const float4*>(part_o + (int64_t)k * stride_rows * dv + c)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    const float l_mine = lane < n ? part_lse[(int64_t)lane * stride_rows] : -INFINITY;
+    float4 x[kSmallMerge];
+    load_chunk(0, x);
+    float m = l_mine;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float w_mine = (m == -INFINITY || l_mine == -INFINITY) ? 0.f : __expf(l_mine - m);
+    float wsum = w_mine;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    float w[kSmallMerge];
+#pragma unroll
+    for (int k = 0; k < kSmallMerge; ++k) w[k] = __shfl_sync(0xffffffffu, w_mine, k);  // 0 past n
+    for (int c0 = 0; c0 < dv; c0 += 128) {
+        if (c0 > 0) load_chunk(c0, x);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kSmallMerge; ++k) {
+            acc.x += w[k] * x[k].x;
+            acc.y += w[k] * x[k].y;
+            acc.z += w[k] * x[k].z;
+            acc.w += w[k] * x[k].w;
+        }
+        const int c = c0 + lane * 4;
+        if (c < dv) {
+            uint2 o;
+            o.x = pack_bf16(acc.x * inv, acc.y * inv);
+            o.y = pack_bf16(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(out_row + c) = o;
+        }
+    }
+    if (lane == 0 && lse_out) *lse_out = (wsum > 0.f) ? m + __logf(wsum) : -INFINITY;
+}
+
 PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int n, int64_t stride_rows,
                                 int dv, __nv_bfloat16* out_row, float* lse_out) {
+    if (n <= kSmallMerge) {
+        merge_rows_warp_small(part_o, part_lse, n, stride_rows, dv, out_row, lse_out);
+        return;
+    }
     const int lane = threadIdx.x & 31;
     float m = -INFINITY;
     float l_mine[4];  // lse of partials lane, lane + 32, ... (n <= 128 kept in registers)
@@ -168,7 +224,7 @@ PKA_DEVICE void merge_rows_warp(const float* part_o, const float* part_lse, int 
 // Decode split-KV reduction: request r with n > 1 splits; its partials are
 // rows (dec_first[r] + s) * Hq + h.
 
-__global__ void __launch_bounds__(256) decode_reduce_kernel(DecodeReduceParams p) {
+__global__ void __launch_bounds__(256, 4) decode_reduce_kernel(DecodeReduceParams p) {
     grid_dep_wait();
     if (p.hdr->dec_num_pairs == 0) return;
     const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -194,7 +250,7 @@ cudaError_t launch_decode_reduce(const DecodeReduceParams& p, int num_sms, cudaS
 // Extend reduction: token i of extend request r has nslot = 1 + chunks
 // partials at rows (ext_base[r] + slot * qlen + i) * Hq + h.
 
-__global__ void __launch_bounds__(256) extend_reduce_kernel(ExtendReduceParams p) {
+__global__ void __launch_bounds__(256, 4) extend_reduce_kernel(ExtendReduceParams p) {
     grid_dep_wait();
     if (p.hdr->fa_num_items == 0) return;
     const int nd = p.num_decodes, ne = p.num_extends;
