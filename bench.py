@@ -255,6 +255,7 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
              ("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20,
               ("fa_fwd.cu", "fa_fwd_prefill_varlen")),
              ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0, ("fa_fwd.cu", "fa_fwd_mixed")),
+             ("mixed_fp8", W.spec_mixed(), "prefill_extend", "tensor", 0, None),
              ("mla_prefill_extend", W.spec_mla_prefill(), "prefill_extend", "tensor", 0,
               ("fa_fwd.cu", "fa_fwd_mla_prefill_extend")),
              ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0,
@@ -271,6 +272,11 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
                "kernels": {k: round(v["avg_ms"], 4) for k, v in stats.items()}}
         if fp8:
             ent["cache"] = f"FP8 E4M3 codes, k_scale {FP8_SCALES[0]}, v_scale {FP8_SCALES[1]}"
+        cd = stats.get("ctx_dequant", {}).get("avg_ms")
+        if cd:  # the extends' context gathered out of the 8-bit cache: codes read, bf16 written
+            ctx = sum(spec.ctx[spec.num_decodes:spec.num_decodes + spec.num_extends])
+            gbytes = ctx * spec.num_kv_heads * (spec.head_dim + spec.head_dim_v) * 3
+            ent["ctx_dequant"] = roofline("hbm", gbytes / (cd * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s", None)
         cw = stats.get("cache_write", {}).get("avg_ms")
         if cw:  # the step's cache write: its own bytes (read + write), its own roofline
             ent["cache_write"] = roofline("hbm", w["cache_write_bytes"] / (cw * 1e-3) / 1e9, peaks["hbm_gbs"],
@@ -465,7 +471,7 @@ def run_ours(args):
 
 
 WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "decode_gqa_fp8": W.spec_decode_gqa,
-             "prefill_varlen": W.spec_prefill, "mixed": W.spec_mixed,
+             "prefill_varlen": W.spec_prefill, "mixed": W.spec_mixed, "mixed_fp8": W.spec_mixed,
              "mla_decode_bs64": W.spec_mla_decode, "mla_prefill_extend": W.spec_mla_prefill,
              # profiling cases: 64 heads (the warp-MMA MLA kernel), and the
              # non-absorbed prefill/extend at a size an ncu replay handles

@@ -138,6 +138,17 @@ PKA_API size_t pka_workspace_size(int num_decodes, int num_extends, int num_pref
                           int max_query_len, int max_seq_len, int context_chunk_tokens);
 
 /*
+ * pka_workspace_size_fp8 -- the same for pka_paged_attn_forward_fp8. With
+ * extends in the batch it adds the gathered context (the extends' cached
+ * positions as bf16, num_extends x ceil(max_seq_len / 128) x 128 rows per kv
+ * head, K and V) and its block table. Returns 0 for hints the 8-bit forward
+ * would reject.
+ */
+PKA_API size_t pka_workspace_size_fp8(int num_decodes, int num_extends, int num_prefills, int num_tokens,
+                                      int num_q_heads, int num_kv_heads, int head_dim, int head_dim_v,
+                                      int max_query_len, int max_seq_len, int context_chunk_tokens);
+
+/*
  * pka_paged_attn_forward -- attention forward of one continuous batch.
  *
  * For new token i of request r (absolute position p = ctx_r + i, where
@@ -208,22 +219,33 @@ PKA_API pka_status pka_paged_attn_forward(const void *q, const void *k_new, cons
  * pka_paged_attn_forward_fp8 -- pka_paged_attn_forward over an 8-bit cache
  * written by pka_cache_write_fp8 (K = k_scale x code, V = v_scale x code).
  *
- * Computes the same definition with those K and V values:
- *     s_j = scale * k_scale * <q[t][h], code_K[j]>,
- *     out[t][h] = v_scale * sum_j softmax(s)_j code_V[j],   lse as before.
- * The codes are widened inside the decode kernel's tile loads (every E4M3
- * value is exactly an f16 value); the products run on f16 operands with
- * float32 accumulation, so q is converted to f16 once per work unit: the call
- * requires |q| < 65504 (larger magnitudes saturate) and rounds q elements
- * below 2^-14 in magnitude to f16's subnormal spacing 2^-24.
+ * Computes the same definition, with these K and V values for the positions
+ * read from the cache ("Beyond porting", absorbed / non-absorbed recipe:
+ * the new tokens' attention runs on the step's own K/V, the context chunks
+ * on the cache after gather_and_maybe_dequant_cache):
+ *   * a decode reads every position from the cache, its own new token
+ *     included (written there by pka_cache_write_fp8 first);
+ *   * an extend reads its cached positions from the cache and its new
+ *     tokens' K/V from k_new / v_new (bf16); a prefill reads only k_new/v_new.
+ * For positions from the cache s_j = scale * k_scale * <q[t][h], code_K[j]>
+ * and their share of out is v_scale * softmax(s)_j code_V[j].
+ *
+ * Decode: the codes are widened inside the decode kernel's tile loads (every
+ * E4M3 value is exactly an f16 value); the products run on f16 operands with
+ * float32 accumulation, so q is converted to f16 once per work unit: decode
+ * queries must satisfy |q| < 65504 (larger magnitudes saturate), and q
+ * elements below 2^-14 in magnitude are rounded to f16's subnormal spacing.
+ * Extend: the extends' cached positions are first gathered into the
+ * workspace as bf16 copies of the codes' values (exact), then the bf16
+ * prefill/extend kernel runs with the scales applied to the context chunks'
+ * scores and outputs.
  *
  * Arguments as in pka_paged_attn_forward, with k_cache / v_cache as uint8 E4M3
  * codes in the same [num_blocks, num_kv_heads, block_size, head_dim] layout and
- * the two scales (finite, > 0). The workspace is sized by the same
- * pka_workspace_size. Supported: decode-only batches (num_extends ==
- * num_prefills == 0), head_dim == head_dim_v == 128, v_cache not NULL,
- * num_q_heads / num_kv_heads <= 16, block_size a power of two in [1, 128];
- * other shapes return PKA_ERR_UNSUPPORTED.
+ * the two scales (finite, > 0). The workspace is sized by
+ * pka_workspace_size_fp8. Supported: head_dim == head_dim_v == 128, v_cache
+ * not NULL, num_q_heads / num_kv_heads <= 16, block_size a power of two in
+ * [1, 128]; other shapes return PKA_ERR_UNSUPPORTED.
  */
 PKA_API pka_status pka_paged_attn_forward_fp8(const void *q, const void *k_new, const void *v_new,
                                               const void *k_cache, const void *v_cache,
@@ -328,7 +350,8 @@ typedef enum {
     PKA_KERNEL_EXTEND_REDUCE = 5,
     PKA_KERNEL_MERGE = 6,
     PKA_KERNEL_GATHER = 7,          /* pka_gather_rows */
-    PKA_KERNEL_COUNT = 8
+    PKA_KERNEL_CTX_DEQUANT = 8,     /* 8-bit cache: the extends' context gather */
+    PKA_KERNEL_COUNT = 9
 } pka_kernel;
 
 /* enable != 0 turns timing on for `kernel` (and resets it); 0 turns it off. */

@@ -35,6 +35,7 @@ cudaError_t launch_gather_rows(void* dst, const void* src, const int32_t* idx, i
                                int64_t row_bytes, int32_t* err, int num_sms, cudaStream_t stream);
 cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bound, int num_sms,
                                  cudaStream_t stream);
+cudaError_t launch_ctx_dequant(const CtxDequantParams& p, cudaStream_t stream);
 int decode_gqa_target_units(int num_sms);
 int decode_mla_heads_per_cta(int Hq);
 bool decode_mla_tc_supported(int Hq);
@@ -149,7 +150,10 @@ int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 struct Hints {
     int nd, ne, np, T, Hq, Hkv, d, dv, maxq, maxs, chunk;
     bool mla;
+    bool fp8 = false;  // 8-bit cache: the extends' context is gathered into the workspace
 };
+
+constexpr int kCtxRows = 128;  // rows of a gathered context block
 
 // Returns false if the hints are not a shape this build supports.
 bool compute_layout(const Hints& h, int num_sms, Layout* L) {
@@ -185,6 +189,16 @@ bool compute_layout(const Hints& h, int num_sms, Layout* L) {
     L->off_dec_part_lse = take(sizeof(float) * (size_t)pair_cap * h.Hq);
     L->off_ext_part_o = take(sizeof(float) * (size_t)row_cap * h.Hq * h.dv);
     L->off_ext_part_lse = take(sizeof(float) * (size_t)row_cap * h.Hq);
+    if (h.fp8 && h.ne > 0) {
+        // every extend's context fits ceil(max_seq_len / 128) blocks
+        const int64_t nblk = (h.maxs + kCtxRows - 1) / kCtxRows;
+        const int64_t rows = (int64_t)h.ne * nblk * kCtxRows * h.Hkv;
+        if (nblk > INT32_MAX / 4 || (int64_t)h.ne * nblk > INT32_MAX / 4 || rows >= (int64_t)INT32_MAX) return false;
+        L->ctx_nblk = (int)nblk;
+        L->off_ctx_k = take(sizeof(uint16_t) * (size_t)rows * h.d);
+        L->off_ctx_v = take(sizeof(uint16_t) * (size_t)rows * h.dv);
+        L->off_ctx_bt = take(sizeof(int32_t) * (size_t)h.ne * nblk);
+    }
     L->total = off;
     return true;
 }
@@ -383,6 +397,24 @@ size_t pka_workspace_size(int num_decodes, int num_extends, int num_prefills, in
     return L.total;
 }
 
+size_t pka_workspace_size_fp8(int num_decodes, int num_extends, int num_prefills, int num_tokens,
+                              int num_q_heads, int num_kv_heads, int head_dim, int head_dim_v, int max_query_len,
+                              int max_seq_len, int context_chunk_tokens) {
+    if (head_dim != 128 || head_dim_v != 128) return 0;  // the 8-bit kernels' head dims
+    bool is_mla = false;
+    if (check_shape(num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads, head_dim,
+                    head_dim_v, max_query_len, max_seq_len, context_chunk_tokens, false, &is_mla) != PKA_OK)
+        return 0;
+    const int sms = device_sm_count();
+    if (sms <= 0) return 0;
+    Hints h{num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads, head_dim,
+            head_dim_v, max_query_len, max_seq_len, context_chunk_tokens, false};
+    h.fp8 = true;
+    Layout L;
+    if (!compute_layout(h, sms, &L)) return 0;
+    return L.total;
+}
+
 }  // extern "C"
 
 namespace {
@@ -413,7 +445,6 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
     if (cf.fp8) {
         // the 8-bit cache: GQA decode-only batches of head dim 128
         if (is_mla || head_dim != 128 || head_dim_v != 128) return PKA_ERR_UNSUPPORTED;
-        if (num_extends + num_prefills > 0) return PKA_ERR_UNSUPPORTED;
         if (!std::isfinite(cf.k_scale) || !(cf.k_scale > 0.f) || !std::isfinite(cf.v_scale) || !(cf.v_scale > 0.f))
             return PKA_ERR_INVALID_ARG;
     }
@@ -436,6 +467,7 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
     if (sms <= 0) return PKA_ERR_CUDA;
     Hints h{num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads, head_dim, head_dim_v,
             max_query_len, max_seq_len, context_chunk_tokens, is_mla};
+    h.fp8 = cf.fp8;
     Layout L;
     if (!compute_layout(h, sms, &L)) return PKA_ERR_UNSUPPORTED;
     if (workspace_bytes < L.total) return PKA_ERR_WORKSPACE_TOO_SMALL;
@@ -473,6 +505,34 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
     pp.ext_base = reinterpret_cast<int32_t*>(ws + L.off_ext_base);
     if ((e = timed(PKA_KERNEL_PLANNER, st, [&] { return launch_planner(pp, st); })) != cudaSuccess)
         return PKA_ERR_CUDA;
+
+    // ---- 8-bit cache with extends: gather their context as bf16 code values
+    // (after the planner, which clears the error word this kernel may set)
+    const bool gathered = cf.fp8 && num_extends > 0;
+    CtxDequantParams cd;
+    std::memset(&cd, 0, sizeof(cd));
+    if (gathered) {
+        cd.k8 = static_cast<const uint8_t*>(k_cache);
+        cd.v8 = static_cast<const uint8_t*>(v_cache);
+        cd.block_table = block_table;
+        cd.qsl = query_start_loc;
+        cd.seq_lens = seq_lens;
+        cd.kc = reinterpret_cast<__nv_bfloat16*>(ws + L.off_ctx_k);
+        cd.vc = reinterpret_cast<__nv_bfloat16*>(ws + L.off_ctx_v);
+        cd.bt_c = reinterpret_cast<int32_t*>(ws + L.off_ctx_bt);
+        cd.err = &hdr->err;
+        cd.num_blocks = num_blocks;
+        cd.max_blocks = max_blocks_per_req;
+        cd.num_decodes = num_decodes;
+        cd.num_extends = num_extends;
+        cd.Hkv = num_kv_heads;
+        cd.bs = block_size;
+        cd.d = head_dim;
+        cd.dv = head_dim_v;
+        cd.nblk = L.ctx_nblk;
+        if ((e = timed(PKA_KERNEL_CTX_DEQUANT, st, [&] { return launch_ctx_dequant(cd, st); })) != cudaSuccess)
+            return PKA_ERR_CUDA;
+    }
 
     const float scale_log2 = scale * 1.4426950408889634f;
     auto* outb = static_cast<__nv_bfloat16*>(out);
@@ -587,9 +647,15 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
         fp.q = static_cast<const __nv_bfloat16*>(q);
         fp.k_new = static_cast<const __nv_bfloat16*>(k_new);
         fp.v_new = static_cast<const __nv_bfloat16*>(v_new);
-        fp.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-        fp.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
-        fp.block_table = block_table;
+        // context chunks: the cache itself, or the gathered bf16 copy of an 8-bit cache
+        const void* kc = gathered ? static_cast<const void*>(cd.kc) : k_cache;
+        const void* vc = gathered ? static_cast<const void*>(cd.vc) : v_cache;
+        const int ctx_bs = gathered ? kCtxRows : block_size;
+        const int64_t ctx_blocks = gathered ? (int64_t)num_extends * L.ctx_nblk : num_blocks;
+        fp.k_cache = static_cast<const __nv_bfloat16*>(kc);
+        fp.v_cache = static_cast<const __nv_bfloat16*>(vc);
+        fp.block_table = gathered ? cd.bt_c : block_table;
+        fp.bt_row0 = gathered ? num_decodes : 0;
         fp.qsl = query_start_loc;
         fp.seq_lens = seq_lens;
         fp.hdr = hdr;
@@ -602,26 +668,29 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
         fp.out = outb;
         fp.out_v8 = aligned(outb, 32) ? 1 : 0;
         fp.lse = lse;
-        fp.num_blocks = num_blocks;
-        fp.max_blocks = max_blocks_per_req;
+        fp.num_blocks = ctx_blocks;
+        fp.max_blocks = gathered ? L.ctx_nblk : max_blocks_per_req;
         fp.Hq = num_q_heads;
         fp.Hkv = num_kv_heads;
         fp.G = num_q_heads / num_kv_heads;
-        fp.bs = block_size;
+        fp.bs = ctx_bs;
         fp.chunk = context_chunk_tokens;
         fp.num_decodes = num_decodes;
         fp.num_extends = num_extends;
         fp.scale_log2 = scale_log2;
+        // an 8-bit cache's scales apply to the context chunks only
+        fp.ctx_scale_log2 = cf.fp8 ? scale_log2 * cf.k_scale : scale_log2;
+        fp.ctx_v_scale = cf.fp8 ? cf.v_scale : 1.f;
         FaMaps maps;
         std::memset(&maps, 0, sizeof(maps));
         if (!encode_tokens(&maps.q, q, (uint64_t)num_tokens, num_q_heads, head_dim) ||
             !encode_tokens(&maps.knew, k_new, (uint64_t)num_tokens, num_kv_heads, head_dim) ||
             !encode_tokens(&maps.vnew, v_new, (uint64_t)num_tokens, num_kv_heads, head_dim_v))
             return PKA_ERR_CUDA;
-        if (block_size >= 8) {
-            const uint32_t br = (uint32_t)std::min(block_size, 128);
-            if (!encode_rows(&maps.kc, k_cache, (uint64_t)cache_rows, head_dim, br) ||
-                !encode_rows(&maps.vc, v_cache, (uint64_t)cache_rows, head_dim_v, br))
+        if (ctx_bs >= 8) {
+            const uint32_t br = (uint32_t)std::min(ctx_bs, 128);
+            const uint64_t rows = (uint64_t)ctx_blocks * num_kv_heads * ctx_bs;
+            if (!encode_rows(&maps.kc, kc, rows, head_dim, br) || !encode_rows(&maps.vc, vc, rows, head_dim_v, br))
                 return PKA_ERR_CUDA;
         }
         if ((e = timed(PKA_KERNEL_PREFILL_EXTEND, st,

@@ -284,6 +284,14 @@ PKA_DEVICE void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32
 }
 
 // Two floats -> bf16x2 (round to nearest even); `lo` lands in the low half.
+// Two E4M3 codes (low byte -> low half) to an f16 pair; exact (every E4M3
+// value is an f16 value).
+PKA_DEVICE uint32_t e4m3x2_to_f16x2(uint32_t x16) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(x16));
+    return d;
+}
+
 PKA_DEVICE uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -62,12 +62,6 @@ struct F8Cfg {
     static constexpr int kSmem = kRingBytes + 1024 + 64 * 8;
 };
 
-// Two E4M3 codes (low byte -> low half) to an f16 pair.
-PKA_DEVICE uint32_t e4m3x2_to_f16x2(uint32_t x16) {
-    uint32_t d;
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(x16));
-    return d;
-}
 PKA_DEVICE uint32_t e4m3_lo(uint32_t w) { return e4m3x2_to_f16x2(w & 0xffffu); }
 PKA_DEVICE uint32_t e4m3_hi(uint32_t w) { return e4m3x2_to_f16x2(w >> 16); }
 

@@ -129,7 +129,9 @@ PKA_DEVICE int tile_block_id(const FaParams& p, const int32_t* bt, int kb, int c
     return blk;
 }
 
-template <int D, int DV>
+// kCtxScaled: the context chunks carry their own score scale and output
+// factor (a gathered 8-bit cache); otherwise every slot uses scale_log2.
+template <int D, int DV, bool kCtxScaled>
 __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_constant__ FaMaps maps, const FaParams p) {
     grid_dep_wait();
     using C = FaCfg<D, DV>;
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                                         c * 64, U.h, U.q0 + U.row0 + k * BM, pol_q);
                 }
             }
-            const int32_t* bt = p.block_table + (int64_t)U.r * p.max_blocks;
+            const int32_t* bt = U.slot != 0 ? p.block_table + (int64_t)(U.r - p.bt_row0) * p.max_blocks : p.block_table;
             const bool paged_tma = U.slot != 0 && ctx_tma;
             int blk_next = paged_tma ? tile_block_id(p, bt, U.kb0, U.c1, lane) : 0;
             bool ok = true;
@@ -402,7 +404,6 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
         const int wg_tid = threadIdx.x - 128 * (k + 1);
         const uint32_t tS = tbase + lane_off + C::kColS + k * 128;
         const uint32_t tO = tbase + lane_off + C::kColO + k * DV;
-        const float sl2 = p.scale_log2;
         uint32_t n_s = 0;  // S tiles of this warpgroup (all units)
         uint32_t kv_it = 0;
         for (int u = blockIdx.x; u < num_units && !warp_flag(s_abort); u += gridDim.x) {
@@ -414,6 +415,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             const int row0 = U.row0 + k * BM;
             const int qi = row0 + row;  // query index within the request's new tokens
             const int c1 = k ? U.c1k[1] : U.c1k[0];
+            const float sl2 = (kCtxScaled && U.slot != 0) ? p.ctx_scale_log2 : p.scale_log2;
             float m_used = -INFINITY, l = 0.f;
             bool ok = true;
             for (int t = 0; t < ntk; ++t) {
@@ -612,7 +614,7 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
             const int64_t orow = final_out ? ((int64_t)(U.q0 + qi) * p.Hq + U.h)
                                            : (((int64_t)p.ext_base[U.r - p.num_decodes] + (int64_t)U.slot * U.qlen + qi) *
                                                   p.Hq + U.h);
-            const float inv = 1.f / l;
+            const float inv = ((kCtxScaled && U.slot != 0) ? p.ctx_v_scale : 1.f) / l;
             // 64 columns per TMEM round trip; each thread writes its own row,
             // 32 bytes (one whole sector) per store where the output allows
 #pragma unroll 1
@@ -675,9 +677,9 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
     }
 }
 
-template <int D, int DV>
+template <int D, int DV, bool kCtxScaled = false>
 static cudaError_t launch_fa_d(const FaMaps& maps, const FaParams& p, int num_sms, cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, DV>;
+    auto kern = fa_fwd_kernel<D, DV, kCtxScaled>;
     const int smem = FaCfg<D, DV>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -686,7 +688,11 @@ static cudaError_t launch_fa_d(const FaMaps& maps, const FaParams& p, int num_sm
 
 cudaError_t launch_fa_fwd(const FaMaps& maps, const FaParams& p, int head_dim, int head_dim_v, int num_sms,
                           cudaStream_t stream) {
-    if (head_dim == 128 && head_dim_v == 128) return launch_fa_d<128, 128>(maps, p, num_sms, stream);
+    const bool scaled = p.ctx_scale_log2 != p.scale_log2 || p.ctx_v_scale != 1.f;
+    if (head_dim == 128 && head_dim_v == 128)
+        return scaled ? launch_fa_d<128, 128, true>(maps, p, num_sms, stream)
+                      : launch_fa_d<128, 128>(maps, p, num_sms, stream);
+    if (scaled) return cudaErrorInvalidValue;  // scaled context chunks: head dim 128 only
     if (head_dim == 64 && head_dim_v == 64) return launch_fa_d<64, 64>(maps, p, num_sms, stream);
     if (head_dim == 192 && head_dim_v == 128) return launch_fa_d<192, 128>(maps, p, num_sms, stream);
     return cudaErrorInvalidValue;

@@ -75,7 +75,28 @@ struct FaParams {
     int64_t num_blocks;
     int max_blocks, Hq, Hkv, G, bs, chunk, num_decodes, num_extends;
     int out_v8;  // out is 32-byte aligned: rows go out in 32-byte stores
+    int bt_row0;  // request of block_table's first row (context chunks only read the table)
     float scale_log2;
+    // context chunks (slots >= 1): score scale and output factor. The plain
+    // bf16 cache: scale_log2 and 1. A gathered 8-bit cache holds the codes'
+    // values: scale_log2 * k_scale and v_scale.
+    float ctx_scale_log2, ctx_v_scale;
+};
+
+// Gather of the extends' context out of an 8-bit cache into a compact bf16
+// cache (ctx_dequant.cu).
+struct CtxDequantParams {
+    const uint8_t* k8;  // [num_blocks, Hkv, bs, d] E4M3 codes
+    const uint8_t* v8;  // [num_blocks, Hkv, bs, dv]
+    const int32_t* block_table;
+    const int32_t* qsl;
+    const int32_t* seq_lens;
+    __nv_bfloat16* kc;  // [num_extends * nblk, Hkv, 128, d]
+    __nv_bfloat16* vc;  // [num_extends * nblk, Hkv, 128, dv]
+    int32_t* bt_c;      // [num_extends, nblk]
+    int32_t* err;
+    int64_t num_blocks;
+    int max_blocks, num_decodes, num_extends, Hkv, bs, d, dv, nblk;
 };
 
 struct DecodeReduceParams {

@@ -41,8 +41,11 @@ static_assert(sizeof(PlanHeader) == 256, "plan header is one 256-byte line");
 struct Layout {
     size_t off_dec_pairs, off_dec_first, off_dec_nsplit, off_fa_items, off_ext_base;
     size_t off_dec_part_o, off_dec_part_lse, off_ext_part_o, off_ext_part_lse;
+    // 8-bit cache with extends: the extends' context gathered as bf16 code
+    // values, ctx_nblk blocks of 128 rows per extend, and its block table
+    size_t off_ctx_k, off_ctx_v, off_ctx_bt;
     size_t total;
-    int dec_pair_cap, fa_item_cap, ext_row_cap, dec_target_units;
+    int dec_pair_cap, fa_item_cap, ext_row_cap, dec_target_units, ctx_nblk;
 };
 
 struct PlanParams {

@@ -100,8 +100,8 @@ class DeviceBatch:
         self.lse = inner.view(torch.float32).view(T, Hq)
         self.max_query_len = int(max(spec.qlen))
         self.max_seq_len = int(max(spec.seq_lens))
-        ws = pka.pka_workspace_size(*self.counts, T, Hq, Hkv, d, dv, self.max_query_len, self.max_seq_len,
-                                    spec.context_chunk)
+        size_fn = pka.pka_workspace_size if kv_scales is None else pka.pka_workspace_size_fp8
+        ws = size_fn(*self.counts, T, Hq, Hkv, d, dv, self.max_query_len, self.max_seq_len, spec.context_chunk)
         if ws == 0:
             raise RuntimeError("pka_workspace_size rejected the batch shape")
         self._ws_buf, self.workspace = guarded_empty(ws, device)

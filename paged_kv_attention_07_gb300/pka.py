@@ -19,13 +19,14 @@ STATUS_NAMES = {0: "PKA_OK", 1: "PKA_ERR_INVALID_ARG", 2: "PKA_ERR_UNSUPPORTED",
 DEVERR = {"QUERY_START_LOC": 0x01, "SEQ_LEN": 0x02, "ORDER": 0x04, "QUERY_LEN": 0x08,
           "BLOCK_TABLE": 0x10, "BLOCK_ID": 0x20, "SLOT": 0x40, "CAPACITY": 0x80, "TIMEOUT": 0x100,
           "INDEX": 0x200}
-EXPORTED = ("pka_cache_write", "pka_cache_write_fp8", "pka_workspace_size", "pka_paged_attn_forward",
+EXPORTED = ("pka_cache_write", "pka_cache_write_fp8", "pka_workspace_size", "pka_workspace_size_fp8",
+            "pka_paged_attn_forward",
             "pka_paged_attn_forward_fp8",
             "pka_merge_attn_states", "pka_get_error", "pka_paged_decode_noalloc", "pka_kernel_timer",
             "pka_kernel_timer_read", "pka_batch_order", "pka_gather_rows", "pka_selftest_wait",
             "pka_status_string")
 KERNELS = {"cache_write": 0, "planner": 1, "decode": 2, "decode_reduce": 3, "prefill_extend": 4,
-           "extend_reduce": 5, "merge": 6, "gather": 7}
+           "extend_reduce": 5, "merge": 6, "gather": 7, "ctx_dequant": 8}
 
 
 class PkaError(RuntimeError):
@@ -61,6 +62,8 @@ def load(path: str | None = None):
                                                i32, i32, i64, i32, f32, f32, f32, i32, i32, i32, P, P, P, sz, P]
     lib.pka_workspace_size.restype = sz
     lib.pka_workspace_size.argtypes = [i32] * 11
+    lib.pka_workspace_size_fp8.restype = sz
+    lib.pka_workspace_size_fp8.argtypes = [i32] * 11
     lib.pka_paged_attn_forward.restype = i32
     lib.pka_paged_attn_forward.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
                                            i32, i32, i64, i32, f32, i32, i32, i32, P, P, P, sz, P]
@@ -134,6 +137,13 @@ def pka_workspace_size(num_decodes, num_extends, num_prefills, num_tokens, num_q
     return int(load().pka_workspace_size(num_decodes, num_extends, num_prefills, num_tokens, num_q_heads,
                                          num_kv_heads, head_dim, head_dim_v, max_query_len, max_seq_len,
                                          context_chunk_tokens))
+
+
+def pka_workspace_size_fp8(num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads,
+                           head_dim, head_dim_v, max_query_len, max_seq_len, context_chunk_tokens) -> int:
+    return int(load().pka_workspace_size_fp8(num_decodes, num_extends, num_prefills, num_tokens, num_q_heads,
+                                             num_kv_heads, head_dim, head_dim_v, max_query_len, max_seq_len,
+                                             context_chunk_tokens))
 
 
 def pka_paged_attn_forward(q, k_new, v_new, k_cache, v_cache, block_table, query_start_loc, seq_lens,

@@ -133,7 +133,10 @@ def test_fp8_entry_points_reject_bad_arguments(lib):
             FAKE, FAKE, FAKE, FAKE, a["vc"], FAKE, 8, FAKE, FAKE, a["nd"], a["ne"], a["np"], a["T"], 8, 2, a["d"],
             a["dv"], 64, 16, ctypes.c_float(0.125), ctypes.c_float(a["ks"]), ctypes.c_float(a["vs"]), 32, 4, 100,
             FAKE, None, P(0x100000), 1 << 20, None)
-    assert fwd(ne=1, T=6) == 2          # extend over an 8-bit cache: no kernel
-    assert fwd(np=1, T=6) == 2          # prefill likewise
     assert fwd(d=64, dv=64) == 2        # head dim 64
+    assert fwd(ne=1, T=6, d=64, dv=64) == 2
+    assert fwd(vc=None, d=576, dv=512) == 2  # a latent (MLA) cache has no 8-bit kernel
+    # the 8-bit workspace query refuses what the 8-bit forward refuses, before any device query
+    assert lib.pka_workspace_size_fp8(1, 1, 1, 8, 8, 2, 64, 64, 6, 100, 32) == 0
+    assert lib.pka_workspace_size_fp8(1, 1, 1, 8, 8, 2, 192, 128, 6, 100, 32) == 0
     assert fwd(ks=0.0) == 1 and fwd(vs=float("inf")) == 1

@@ -1,7 +1,9 @@
 """GPU parity of the 8-bit (FP8 E4M3) KV cache: the quantising cache write
 bit for bit against the oracle's codes (float32 quotient, nearest code, ties
-to even, saturation), and the decode over the codes against the oracle's
-attention on the codes' exact values with the scales taken out of the sums."""
+to even, saturation), and the forward over the codes against the oracle's
+8-bit step: decodes read every position from the codes, extends their
+cached positions (gathered into the workspace) with their new tokens from
+k_new / v_new, prefills only k_new / v_new."""
 import numpy as np
 import pytest
 
@@ -44,8 +46,9 @@ def check_fp8(batch, k_scale=K_SCALE, v_scale=V_SCALE):
     assert np.array_equal(db.k_cache.cpu().numpy(), kc)
     assert np.array_equal(db.v_cache.cpu().numpy(), vc)
     spec = batch.spec
-    ref_o, ref_l = fp8.attention_fp8(batch.q, kc, vc, k_scale, v_scale, batch.block_table, batch.query_start_loc,
-                                     batch.seq_lens, spec.scale, spec.block_size, head_dim_v=spec.head_dim_v)
+    ref_o, ref_l = fp8.step_reference_fp8(batch.q, kc, vc, batch.k_new, batch.v_new, k_scale, v_scale,
+                                          batch.block_table, batch.query_start_loc, batch.seq_lens,
+                                          spec.num_decodes, spec.scale, spec.block_size)
     out = db.out.float().cpu().numpy().reshape(-1, spec.head_dim_v)
     lse = db.lse.cpu().numpy().reshape(-1)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
@@ -120,15 +123,41 @@ def test_fp8_cache_write_rounding_cases():
     assert ref_k[0, 0, 0, :12].tolist() == [0x38, 0x3A, 0xB8, 0x7E, 0xFE, 0x00, 0x02, 0x00, 0x80, 0x7E, 0x7E, 0x00]
 
 
-def test_fp8_forward_rejects_unsupported():
+@pytest.mark.parametrize("bs,chunk", [(16, 64), (1, 48), (64, 1000), (128, 128), (8, 32768)])
+def test_fp8_mixed_step(bs, chunk):
+    """Decodes, extends (context over several chunks, ragged tails) and
+    prefills in one step over an 8-bit cache."""
+    spec = W.spec_custom(f"f8_mix{bs}_{chunk}", ctx=[7, 300, 1100, 129, 700, 255, 0, 0],
+                         qlen=[1, 1, 1, 40, 130, 3, 200, 17], num_decodes=3, num_extends=3, num_prefills=2,
+                         Hq=16, Hkv=2, d=128, dv=128, bs=bs, chunk=chunk, seed=400 + bs)
+    check_fp8(W.make_batch(spec))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (32, 4), (12, 4)])
+def test_fp8_extend_only(Hq, Hkv):
+    spec = W.spec_custom(f"f8_ext{Hq}", ctx=[1, 64, 500, 2000], qlen=[5, 256, 70, 129], num_decodes=0,
+                         num_extends=4, num_prefills=0, Hq=Hq, Hkv=Hkv, d=128, dv=128, bs=16, chunk=512,
+                         seed=410 + Hq)
+    check_fp8(W.make_batch(spec))
+
+
+def test_fp8_prefill_only():
+    spec = W.spec_custom("f8_pre", ctx=[0, 0, 0], qlen=[1, 300, 129], num_decodes=0, num_extends=0,
+                         num_prefills=3, Hq=8, Hkv=2, d=128, dv=128, bs=16, seed=420)
+    check_fp8(W.make_batch(spec))
+
+
+def test_fp8_one_token_extends():
+    """Requests with one new token routed through the extend slice read
+    their context from the gathered cache and their own token from k_new."""
+    spec = W.spec_custom("f8_uni", ctx=[10, 900, 33], qlen=[1, 1, 1], num_decodes=0, num_extends=3,
+                         num_prefills=0, Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=256, seed=430)
+    check_fp8(W.make_batch(spec))
+
+
+def test_fp8_unsupported_shapes_are_refused():
     """Shapes the 8-bit path has no kernel for are refused before any launch."""
-    import torch
     from paged_kv_attention_07_gb300 import pka
-    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
-    spec = W.spec_custom("f8_ext", ctx=[10, 40], qlen=[1, 5], num_decodes=1, num_extends=1, num_prefills=0,
-                         Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=32, seed=3)
-    db = DeviceBatch(W.make_batch(spec), kv_scales=(K_SCALE, V_SCALE))
-    with pytest.raises(pka.PkaError) as ei:
-        db.forward()
-    assert ei.value.status == 2
-    torch.cuda.synchronize()
+    assert pka.pka_workspace_size_fp8(1, 1, 1, 8, 8, 2, 64, 64, 6, 100, 32) == 0
+    assert pka.pka_workspace_size_fp8(1, 1, 1, 8, 8, 2, 192, 128, 6, 100, 32) == 0
+    assert pka.pka_workspace_size_fp8(1, 1, 1, 8, 8, 2, 128, 128, 6, 100, 32) > 0
