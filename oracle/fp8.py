@@ -16,15 +16,22 @@ import numpy as np
 MAX_FINITE = 448.0
 
 
-def decode(codes) -> np.ndarray:
-    """float64 value of each 8-bit code (NaN for the two NaN codes)."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+def _decode_definition(c: np.ndarray) -> np.ndarray:
+    """The format's definition, applied to int64 codes."""
     sign = np.where(c & 0x80, -1.0, 1.0)
     e = (c >> 3) & 0xF
     m = (c & 0x7).astype(np.float64)
     mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
     out = sign * mag
     return np.where((c & 0x7F) == 0x7F, np.nan, out)
+
+
+_VALUE = _decode_definition(np.arange(256, dtype=np.int64))  # value of every code
+
+
+def decode(codes) -> np.ndarray:
+    """float64 value of each 8-bit code (NaN for the two NaN codes)."""
+    return _VALUE[np.asarray(codes, dtype=np.uint8)]
 
 
 _POS = decode(np.arange(0x7F))  # the 127 non-negative finite values, ascending with the code
@@ -93,7 +100,7 @@ def _bf16_bits_to_f64(bits) -> np.ndarray:
 
 
 def step_reference_fp8(q, k_codes, v_codes, k_new, v_new, k_scale, v_scale, block_table, query_start_loc,
-                       seq_lens, num_decodes, scale, block_size):
+                       seq_lens, num_decodes, scale, block_size, rows=None):
     """One step over an 8-bit cache, float64, written out per request and head.
 
     Which values a query sees (the pages' prefill listing: the new tokens'
@@ -109,18 +116,19 @@ def step_reference_fp8(q, k_codes, v_codes, k_new, v_new, k_scale, v_scale, bloc
     lse = log sum_j e^{s_j}, out = sum_j e^{s_j - lse} V_j.
 
     q, k_new, v_new: bf16 bits [T, H, d]; k_codes / v_codes: uint8
-    [blocks, Hkv, bs, d]. Returns (out [T * Hq, dv], lse [T * Hq]) in the
-    flattened row order t * Hq + h."""
-    qf = _bf16_bits_to_f64(q)
-    kn, vn = _bf16_bits_to_f64(k_new), _bf16_bits_to_f64(v_new)
-    T, Hq, d = qf.shape
+    [blocks, Hkv, bs, d]. Returns (out, lse) for `rows` (flattened t * Hq + h,
+    default every row in order)."""
+    q = np.asarray(q)
+    T, Hq, d = q.shape
     Hkv, dv = k_codes.shape[1], v_codes.shape[3]
     G = Hq // Hkv
-    kdec, vdec = dequantize(k_codes, k_scale), dequantize(v_codes, v_scale)
-    out = np.zeros((T, Hq, dv))
-    lse = np.zeros((T, Hq))
+    rows = np.arange(T * Hq, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.size, dv))
+    lse = np.zeros(rows.size)
     qsl = np.asarray(query_start_loc, dtype=np.int64)
-    for r in range(len(seq_lens)):
+    row_t, row_h = rows // Hq, rows % Hq
+    row_r = np.searchsorted(qsl, row_t, side="right") - 1  # request of each row
+    for r in np.unique(row_r):
         t0, t1 = int(qsl[r]), int(qsl[r + 1])
         n, s = t1 - t0, int(seq_lens[r])
         ctx = s - n
@@ -128,19 +136,21 @@ def step_reference_fp8(q, k_codes, v_codes, k_new, v_new, k_scale, v_scale, bloc
         pos = np.arange(cached)
         blk = np.asarray(block_table[r], dtype=np.int64)[pos // block_size]
         for hk in range(Hkv):
-            K = kdec[blk, hk, pos % block_size]
-            V = vdec[blk, hk, pos % block_size]
+            mine = np.nonzero((row_r == r) & (row_h // G == hk))[0]
+            if mine.size == 0:
+                continue
+            K = dequantize(k_codes[blk, hk, pos % block_size], k_scale)
+            V = dequantize(v_codes[blk, hk, pos % block_size], v_scale)
             if cached < s:
-                K = np.concatenate([K, kn[t0:t1, hk]])
-                V = np.concatenate([V, vn[t0:t1, hk]])
-            for g in range(G):
-                h = hk * G + g
-                sc = scale * (qf[t0:t1, h] @ K.T)  # [n, s]
-                visible = np.arange(s)[None, :] <= (ctx + np.arange(n))[:, None]
-                sc = np.where(visible, sc, -np.inf)
-                m = sc.max(axis=1, keepdims=True)
+                K = np.concatenate([K, _bf16_bits_to_f64(k_new[t0:t1, hk])])
+                V = np.concatenate([V, _bf16_bits_to_f64(v_new[t0:t1, hk])])
+            for i in mine:
+                t, h = int(row_t[i]), int(row_h[i])
+                vis = ctx + (t - t0) + 1  # keys 0 .. ctx + (t - t0)
+                sc = scale * (K[:vis] @ _bf16_bits_to_f64(q[t, h]))
+                m = sc.max()
                 e = np.exp(sc - m)
-                den = e.sum(axis=1, keepdims=True)
-                out[t0:t1, h] = (e @ V) / den
-                lse[t0:t1, h] = (m + np.log(den))[:, 0]
-    return out.reshape(T * Hq, dv), lse.reshape(T * Hq)
+                den = e.sum()
+                out[i] = (e @ V[:vis]) / den
+                lse[i] = m + np.log(den)
+    return out, lse

@@ -7,7 +7,6 @@ k_new / v_new, prefills only k_new / v_new."""
 import numpy as np
 import pytest
 
-import oracle
 from oracle import fp8
 from paged_kv_attention_07_gb300 import workloads as W
 from tests.gpu_util import LSE_ATOL, OUT_ATOL
@@ -17,15 +16,35 @@ pytestmark = pytest.mark.gpu
 K_SCALE, V_SCALE = 0.0125, 0.02
 
 
+_CODE_TABLES = {}
+
+
 def _codes_of(bits, scale):
-    return fp8.quantize_f32(W.bf16_bits_to_f32(bits), scale)
+    """Codes of bf16 values: the oracle's float32-quotient quantiser applied
+    once to every bf16 bit pattern, then looked up."""
+    if scale not in _CODE_TABLES:
+        every = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+        with np.errstate(invalid="ignore"):  # the NaN patterns encode to the NaN code
+            _CODE_TABLES[scale] = fp8.quantize_f32(W.bf16_bits_to_f32(every), scale)
+    return _CODE_TABLES[scale][np.asarray(bits, dtype=np.uint16)]
 
 
 def oracle_fp8_cache(batch, k_scale, v_scale):
     """The oracle's 8-bit caches after the step's cache write: every position
-    (context and new tokens) quantised, every other slot the NaN code."""
-    kc, vc = oracle.populate_cache(batch, "all")
-    return _codes_of(kc, k_scale), _codes_of(vc, v_scale)
+    (context and new tokens) quantised, every other slot the NaN code.
+    Quantised request by request (bounded host memory at full size)."""
+    spec = batch.spec
+    shape = (batch.num_blocks, spec.num_kv_heads, spec.block_size)
+    kc = np.full(shape + (spec.head_dim,), 0x7F, np.uint8)
+    vc = np.full(shape + (spec.head_dim_v,), 0x7F, np.uint8)
+    for r in range(spec.num_reqs):
+        a, b = int(batch.seq_start[r]), int(batch.seq_start[r + 1])
+        blk, off = batch.slot_all[a:b] // spec.block_size, batch.slot_all[a:b] % spec.block_size
+        k, v = _codes_of(batch.k_seq[a:b], k_scale), _codes_of(batch.v_seq[a:b], v_scale)
+        for hk in range(spec.num_kv_heads):
+            kc[blk, hk, off] = k[:, hk]
+            vc[blk, hk, off] = v[:, hk]
+    return kc, vc
 
 
 def run_fp8(batch, k_scale=K_SCALE, v_scale=V_SCALE):
@@ -38,19 +57,24 @@ def run_fp8(batch, k_scale=K_SCALE, v_scale=V_SCALE):
     return db
 
 
-def check_fp8(batch, k_scale=K_SCALE, v_scale=V_SCALE):
+def check_fp8(batch, k_scale=K_SCALE, v_scale=V_SCALE, rows=None):
     db = run_fp8(batch, k_scale, v_scale)
     assert db.error_word() == 0
-    kc, vc = oracle_fp8_cache(batch, k_scale, v_scale)
-    # the cache the kernel read is exactly the oracle's codes
-    assert np.array_equal(db.k_cache.cpu().numpy(), kc)
-    assert np.array_equal(db.v_cache.cpu().numpy(), vc)
     spec = batch.spec
-    ref_o, ref_l = fp8.step_reference_fp8(batch.q, kc, vc, batch.k_new, batch.v_new, k_scale, v_scale,
-                                          batch.block_table, batch.query_start_loc, batch.seq_lens,
-                                          spec.num_decodes, spec.scale, spec.block_size)
     out = db.out.float().cpu().numpy().reshape(-1, spec.head_dim_v)
     lse = db.lse.cpu().numpy().reshape(-1)
+    k_dev, v_dev = db.k_cache.cpu().numpy(), db.v_cache.cpu().numpy()
+    del db
+    kc, vc = oracle_fp8_cache(batch, k_scale, v_scale)
+    # the cache the kernel read is exactly the oracle's codes
+    assert np.array_equal(k_dev, kc)
+    assert np.array_equal(v_dev, vc)
+    del k_dev, v_dev
+    ref_o, ref_l = fp8.step_reference_fp8(batch.q, kc, vc, batch.k_new, batch.v_new, k_scale, v_scale,
+                                          batch.block_table, batch.query_start_loc, batch.seq_lens,
+                                          spec.num_decodes, spec.scale, spec.block_size, rows=rows)
+    if rows is not None:
+        out, lse = out[rows], lse[rows]
     assert np.isfinite(out).all() and np.isfinite(lse).all()
     eo, el = np.abs(out - ref_o).max(), np.abs(lse - ref_l).max()
     assert eo <= OUT_ATOL and el <= LSE_ATOL, (eo, el)
@@ -121,6 +145,17 @@ def test_fp8_cache_write_rounding_cases():
     assert np.array_equal(vc.cpu().numpy(), ref_v)
     # the first row's codes, spelled out: ties to even, saturation, subnormal ties, signed zero
     assert ref_k[0, 0, 0, :12].tolist() == [0x38, 0x3A, 0xB8, 0x7E, 0xFE, 0x00, 0x02, 0x00, 0x80, 0x7E, 0x7E, 0x00]
+
+
+@pytest.mark.slow
+def test_fp8_mixed_full():
+    """The mixed workload (128 decodes, 8 extends with up to 100K context in
+    32K chunks, 4 prefills) over an 8-bit cache, in the benchmark's launch
+    configuration: the whole cache bit for bit, every decode row, the first
+    and last token of every request and a seeded sample of other rows."""
+    from tests.gpu_util import sample_rows
+    batch = W.make_batch(W.spec_mixed())
+    check_fp8(batch, rows=sample_rows(batch, 4096, seed=4))
 
 
 @pytest.mark.parametrize("bs,chunk", [(16, 64), (1, 48), (64, 1000), (128, 128), (8, 32768)])
