@@ -37,6 +37,7 @@ cudaError_t launch_extend_reduce(const ExtendReduceParams& p, int ext_tokens_bou
                                  cudaStream_t stream);
 cudaError_t launch_ctx_dequant(const CtxDequantParams& p, cudaStream_t stream);
 int decode_gqa_target_units(int num_sms);
+int decode_gqa_fp8_target_units(int num_sms);
 int decode_mla_heads_per_cta(int Hq);
 bool decode_mla_tc_supported(int Hq);
 cudaError_t launch_decode_mla_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, const CUtensorMap& gmap,
@@ -165,7 +166,9 @@ bool compute_layout(const Hints& h, int num_sms, Layout* L) {
         return o;
     };
     const int upp = h.mla ? mla_units_per_pair(h.Hq) : h.Hkv;
-    L->dec_target_units = h.mla ? num_sms * 4 : decode_gqa_target_units(num_sms);
+    L->dec_target_units = h.mla  ? num_sms * 4
+                          : h.fp8 ? decode_gqa_fp8_target_units(num_sms)
+                                  : decode_gqa_target_units(num_sms);
     if (L->dec_target_units < 1) L->dec_target_units = 1;
     const int64_t pair_cap = h.nd > 0 ? (int64_t)L->dec_target_units / upp + h.nd + 1 : 0;
     int64_t item_cap = 0, row_cap = 0;
