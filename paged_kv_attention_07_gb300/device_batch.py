@@ -107,6 +107,54 @@ class DeviceBatch:
         self._ws_buf, self.workspace = guarded_empty(ws, device)
         torch.cuda.synchronize()
 
+    INPUTS = ("q", "k_new", "v_new", "slot_mapping", "qsl", "seq_lens", "block_table")
+
+    def pack_io(self):
+        """Move the step's inputs into one contiguous device arena, and out and
+        lse into one guarded buffer (each piece 256-byte aligned), so a host
+        loop moves a step's inputs with one copy and its results with another
+        (what a server does with persistent staging buffers). Returns
+        (input arena, output span): uint8 views covering exactly those bytes."""
+        def place(names):
+            offs, off = {}, 0
+            for n in names:
+                t = getattr(self, n)
+                if t is None:
+                    continue
+                offs[n] = off
+                off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+            return offs, off
+        offs, total = place(self.INPUTS)
+        arena = torch.empty(total, dtype=torch.uint8, device=self.device)
+        for n, o in offs.items():
+            t = getattr(self, n)
+            nbytes = t.numel() * t.element_size()
+            view = arena[o:o + nbytes].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            setattr(self, n, view)
+        self._in_offs = offs
+        T, Hq, dv = self.out.shape
+        lse_off = (T * Hq * dv * 2 + 255) // 256 * 256
+        span = lse_off + T * Hq * 4
+        self._out_buf, inner = guarded_empty(span, self.device)
+        self._lse_off = lse_off
+        self.out = inner[:T * Hq * dv * 2].view(torch.bfloat16).view(T, Hq, dv)
+        self.lse = inner[lse_off:span].view(torch.float32).view(T, Hq)
+        self._lse_buf = self._out_buf
+        torch.cuda.synchronize()
+        return arena, inner
+
+    def use_io(self, arena: torch.Tensor, outs: torch.Tensor):
+        """Point the step at another input arena and output span laid out as
+        pack_io's (double buffering: the next step's inputs arrive while this
+        one runs)."""
+        for n, o in self._in_offs.items():
+            t = getattr(self, n)
+            setattr(self, n, arena[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape))
+        T, Hq, dv = self.out.shape
+        self.out = outs[:T * Hq * dv * 2].view(torch.bfloat16).view(T, Hq, dv)
+        self.lse = outs[self._lse_off:self._lse_off + T * Hq * 4].view(torch.float32).view(T, Hq)
+
     def canaries_intact(self) -> bool:
         """True when no byte next to out, lse or the workspace was written."""
         torch.cuda.synchronize()

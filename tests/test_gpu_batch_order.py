@@ -124,3 +124,31 @@ def test_graph_replays_new_metadata():
         assert np.isfinite(o).all() and np.isfinite(l).all(), spec.name
         eo, el = np.abs(o - ref_o).max(), np.abs(l - ref_l).max()
         assert eo <= OUT_ATOL and el <= LSE_ATOL, (spec.name, eo, el)
+
+
+def test_packed_staging_buffers_give_the_same_step():
+    """The inputs moved into one device arena and out / lse into one buffer
+    (the layout the end-to-end benchmark copies with one transfer each way):
+    the step from host-staged inputs matches the oracle and the unpacked step
+    bit for bit, and nothing is written past the outputs."""
+    spec = W.spec_custom("packed", ctx=[40, 300, 70, 0], qlen=[1, 1, 30, 50], num_decodes=2, num_extends=1,
+                         num_prefills=1, Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=64, seed=77)
+    batch = W.make_batch(spec)
+    db = DeviceBatch(batch)
+    db.step()
+    out0, lse0 = db.out.clone(), db.lse.clone()
+    arena, outs = db.pack_io()
+    host_in = arena.cpu().pin_memory()
+    arena.zero_()
+    arena.copy_(host_in, non_blocking=True)
+    db.step()
+    host_out = outs.cpu()
+    torch.cuda.synchronize()
+    assert db.error_word() == 0 and db.canaries_intact()
+    assert torch.equal(db.out, out0) and torch.equal(db.lse, lse0)
+    T, Hq, dv = spec.num_tokens, spec.num_q_heads, spec.head_dim_v
+    out = host_out[:T * Hq * dv * 2].view(torch.bfloat16).float().numpy().reshape(-1, dv)
+    lse_off = (T * Hq * dv * 2 + 255) // 256 * 256
+    lse = host_out[lse_off:lse_off + T * Hq * 4].view(torch.float32).numpy().reshape(-1)
+    ref_o, ref_l = oracle.batch_reference(batch)
+    assert np.abs(out - ref_o).max() <= OUT_ATOL and np.abs(lse - ref_l).max() <= LSE_ATOL
