@@ -341,6 +341,19 @@ PKA_DEVICE float fast_exp2(float x) {
     return y;
 }
 
+// ---------------------------------------------------------------- register split
+// A warpgroup's register budget changes by role: every warp of the warpgroup
+// executes the same instruction; increases draw on what decreases released
+// from the block's launch allocation.
+template <int kRegs>
+PKA_DEVICE void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+PKA_DEVICE void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ---------------------------------------------------------------- dependent launches
 // The forward pass is a chain of kernels on one stream. Each kernel after the
 // planner is launched as a programmatic dependent (launch_dependent below):

@@ -50,6 +50,8 @@
 namespace pka {
 
 constexpr int kFaThreads = 384;
+constexpr int kFaRegsLaunch = 168, kFaRegsIssue = 80, kFaRegsSoftmax = 208;
+static_assert(128 * kFaRegsIssue + 256 * kFaRegsSoftmax <= kFaThreads * kFaRegsLaunch, "register split");
 constexpr int BM = kFaBlockM;  // 128 query rows per query tile
 constexpr int BN = kFaBlockN;  // 128 keys per tile
 static_assert(BM == 128 && BN == 128 && kFaItemTiles == 2, "tile shape is fixed by the TMEM lane count");
@@ -190,213 +192,220 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tbase = s_tmem;
     const uint32_t sm_base = smem_u32(smem);
+    // Registers by role (the launch gives every thread kFaRegsLaunch): the copy
+    // and MMA-issuing warpgroup drops to kFaRegsIssue, the two softmax
+    // warpgroups take what it frees (128 * 80 + 256 * 208 <= 384 * 168).
 
-    if (warp == 0 || warp == 2) {
-        // ------------------------------------------------------------ producers
-        // warp 0 loads K tiles, warp 2 the query tiles and V tiles (so a V load
-        // that waits for an older P . V never delays the next K). K/V lines
-        // stay in L2 with normal priority: every context chunk is read by all
-        // the query heads of its KV head and all query tiles of its request.
-        const int which = warp == 0 ? 0 : 1;  // 0 = K, 1 = V (+ Q)
-        const uint64_t pol_kv = policy_evict_normal();
-        const uint64_t pol_q = policy_evict_last();
-        const bool ctx_tma = p.bs >= 8;
-        uint32_t kv_it = 0, q_it = 0;
-        uint32_t last[2] = {0, 0};  // phase + 1 of the last copy per stage (0 = none)
-        FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
-        for (int u = blockIdx.x; u < num_units && !warp_flag(s_abort); u += gridDim.x, ++q_it) {
-            const FaUnit U = Un;
-            if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);  // prefetch
-            if (which == 1) {
-                // the previous unit's S products are done with the query tiles
-                if (q_it > 0 && !mbar_wait_warp(q_empty, (q_it - 1) & 1, p.err)) {
-                    s_abort = 1;
-                    break;
-                }
-                if (lane == 0) {
-                    const int nq = U.ntk[1] > 0 ? 2 : 1;
-                    mbar_arrive_expect_tx(q_full, (uint32_t)(nq * C::kQBytes));
-                    for (int k = 0; k < nq; ++k)
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_3d(smem + C::kOffQ + k * C::kQBytes + c * C::kChunkBytes, &maps.q, q_full,
-                                        c * 64, U.h, U.q0 + U.row0 + k * BM, pol_q);
-                }
-            }
-            const int32_t* bt = U.slot != 0 ? p.block_table + (int64_t)(U.r - p.bt_row0) * p.max_blocks : p.block_table;
-            const bool paged_tma = U.slot != 0 && ctx_tma;
-            int blk_next = paged_tma ? tile_block_id(p, bt, U.kb0, U.c1, lane) : 0;
-            bool ok = true;
-            const int nstage = which ? C::kVStages : 2;
-            const int nchunk = which ? C::kVChunks : C::kChunks;
-            const int width = which ? DV : D;  // elements per row
-            for (int t = 0; t < U.nkv && ok; ++t, ++kv_it) {
-                const int st = (int)(kv_it % nstage);
-                const uint32_t n = kv_it / nstage;
-                const int kb = U.kb0 + t * BN;
-                const int blk_mine = blk_next;  // block ids of this tile, one per lane
-                if (paged_tma && t + 1 < U.nkv) blk_next = tile_block_id(p, bt, kb + BN, U.c1, lane);
-                uint64_t* full = which ? &v_full[st] : &k_full[st];
-                uint64_t* empty = which ? &v_empty[st] : &k_empty[st];
-                if (n > 0 && !mbar_wait_warp(empty, (n - 1) & 1, p.err)) {
-                    s_abort = 1;
-                    ok = false;
-                    continue;
-                }
-                uint8_t* dst = smem + (which ? C::kOffV + st * C::kVBytes : C::kOffK + st * C::kKBytes);
-                if (U.slot == 0) {
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(full, (uint32_t)(nchunk * C::kChunkBytes));
-                        for (int c = 0; c < nchunk; ++c)
-                            tma_load_3d(dst + c * C::kChunkBytes, which ? &maps.vnew : &maps.knew, full, c * 64, U.g,
-                                        U.q0 + kb, pol_kv);
-                    }
-                } else if (ctx_tma) {
-                    // one lane per block issues that block's boxes (in parallel)
-                    const int bs = p.bs;
-                    const int nvalid = min(BN / bs, (U.c1 - kb + bs - 1) / bs);
-                    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nvalid * nchunk * bs * 128));
-                    __syncwarp();
-                    if (lane < nvalid) {
-                        const int row = (blk_mine * p.Hkv + U.g) * bs;
-                        for (int c = 0; c < nchunk; ++c)
-                            tma_load_2d(dst + c * C::kChunkBytes + lane * bs * 128, which ? &maps.vc : &maps.kc, full,
-                                        c * 64, row, pol_kv);
-                    }
-                } else {
-                    // small blocks: 16-byte copies, rows past the chunk end zero-filled
-                    const uint32_t dbase = smem_u32(dst);
-                    const __nv_bfloat16* src_base = which ? p.v_cache : p.k_cache;
-                    for (int ci = lane; ci < BN * (width / 8); ci += 32) {
-                        const int row = ci / (width / 8), c = ci % (width / 8);
-                        const int pos = kb + row;
-                        const bool valid = pos < U.c1;
-                        int blk = valid ? __ldg(bt + pos / p.bs) : 0;
-                        if (blk < 0 || blk >= p.num_blocks) {
-                            set_error(p.err, PKA_DEVERR_BLOCK_ID);
-                            blk = 0;
-                        }
-                        const int64_t grow = ((int64_t)blk * p.Hkv + U.g) * p.bs + (valid ? pos % p.bs : 0);
-                        cp_async_16_zfill(dbase + (c >> 3) * C::kChunkBytes + sw128(row, c & 7),
-                                          src_base + grow * width + c * 8, valid);
-                    }
-                    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(full)) : "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(full);
-                }
-                last[st] = n + 1;
-            }
-            if (!ok) break;
-        }
-        // no copy may outlive the CTA: wait (bounded) for the last one per stage
-        for (int st = 0; st < (which ? C::kVStages : 2); ++st)
-            if (last[st]) mbar_wait_warp(which ? &v_full[st] : &k_full[st], (last[st] - 1) & 1, p.err);
-        if (which == 1 && q_it > 0) mbar_wait_warp(q_full, (q_it - 1) & 1, p.err);
-    } else if (warp == 1 || warp == 3) {
-        // ------------------------------------------------------------ MMA issuers
-        // warp 1 issues S_k = Q_k K^T for both query tiles of every K tile, each
-        // once the previous P_k . V (which read P_k out of S_k's columns) is
-        // done; warp 3 issues O_k += P_k V as each P_k lands. Each thread
-        // commits only its own MMAs.
-        if (lane == 0 && warp == 1) {
-            constexpr uint32_t idesc_qk = umma_idesc_bf16(128, 128, 0, 0);
-            const uint32_t q_s = sm_base + C::kOffQ, k_s = sm_base + C::kOffK;
+    if (warp < 4) {
+        setmaxnreg_dec<kFaRegsIssue>();
+        if (warp == 0 || warp == 2) {
+            // ------------------------------------------------------------ producers
+            // warp 0 loads K tiles, warp 2 the query tiles and V tiles (so a V load
+            // that waits for an older P . V never delays the next K). K/V lines
+            // stay in L2 with normal priority: every context chunk is read by all
+            // the query heads of its KV head and all query tiles of its request.
+            const int which = warp == 0 ? 0 : 1;  // 0 = K, 1 = V (+ Q)
+            const uint64_t pol_kv = policy_evict_normal();
+            const uint64_t pol_q = policy_evict_last();
+            const bool ctx_tma = p.bs >= 8;
             uint32_t kv_it = 0, q_it = 0;
-            uint32_t nq[2] = {0, 0};  // products issued into S_k
-            bool ok = true;
+            uint32_t last[2] = {0, 0};  // phase + 1 of the last copy per stage (0 = none)
             FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
-            for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x, ++q_it) {
+            for (int u = blockIdx.x; u < num_units && !warp_flag(s_abort); u += gridDim.x, ++q_it) {
                 const FaUnit U = Un;
-                if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
-                if (!mbar_wait(q_full, q_it & 1, p.err)) {
-                    ok = false;
-                    break;
-                }
-                for (int t = 0; t < U.nkv; ++t, ++kv_it) {
-                    const int st = kv_it & 1;
-                    if (!mbar_wait(&k_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
-                    // query tile 0 has no S of this tile: tile 1's product of the
-                    // previous tile may go now (its next S below waits for it)
-                    if (t > 0 && t >= U.ntk[0]) s_qk0_next = (int)kv_it;
-                    for (int k = 0; k < 2; ++k) {
-                        if (t >= U.ntk[k]) continue;
-                        if (nq[k] > 0 && !mbar_wait(&pv_done[k], (nq[k] - 1) & 1, p.err)) { ok = false; break; }
-                        tc_fence_after();
-#pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-                            umma_bf16(tbase + C::kColS + k * 128,
-                                      umma_desc_sw128(q_s + k * C::kQBytes + off, 16, 1024),
-                                      umma_desc_sw128(k_s + st * C::kKBytes + off, 16, 1024), idesc_qk,
-                                      ks > 0 ? 1u : 0u);
-                        }
-                        umma_commit(&s_full[k]);
-                        ++nq[k];
-                        // query tile 0's S of this tile is issued: query tile 1's
-                        // product of the previous tile may go
-                        if (k == 0 && t > 0) s_qk0_next = (int)kv_it;
+                if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);  // prefetch
+                if (which == 1) {
+                    // the previous unit's S products are done with the query tiles
+                    if (q_it > 0 && !mbar_wait_warp(q_empty, (q_it - 1) & 1, p.err)) {
+                        s_abort = 1;
+                        break;
                     }
-                    if (!ok) break;
-                    umma_commit(&k_empty[st]);
-                    if (t == U.nkv - 1) umma_commit(q_empty);
+                    if (lane == 0) {
+                        const int nq = U.ntk[1] > 0 ? 2 : 1;
+                        mbar_arrive_expect_tx(q_full, (uint32_t)(nq * C::kQBytes));
+                        for (int k = 0; k < nq; ++k)
+                            for (int c = 0; c < C::kChunks; ++c)
+                                tma_load_3d(smem + C::kOffQ + k * C::kQBytes + c * C::kChunkBytes, &maps.q, q_full,
+                                            c * 64, U.h, U.q0 + U.row0 + k * BM, pol_q);
+                    }
                 }
-                if (ok) s_qk0_next = (int)kv_it;  // the unit's last tile: nothing of query tile 0 follows
+                const int32_t* bt = U.slot != 0 ? p.block_table + (int64_t)(U.r - p.bt_row0) * p.max_blocks : p.block_table;
+                const bool paged_tma = U.slot != 0 && ctx_tma;
+                int blk_next = paged_tma ? tile_block_id(p, bt, U.kb0, U.c1, lane) : 0;
+                bool ok = true;
+                const int nstage = which ? C::kVStages : 2;
+                const int nchunk = which ? C::kVChunks : C::kChunks;
+                const int width = which ? DV : D;  // elements per row
+                for (int t = 0; t < U.nkv && ok; ++t, ++kv_it) {
+                    const int st = (int)(kv_it % nstage);
+                    const uint32_t n = kv_it / nstage;
+                    const int kb = U.kb0 + t * BN;
+                    const int blk_mine = blk_next;  // block ids of this tile, one per lane
+                    if (paged_tma && t + 1 < U.nkv) blk_next = tile_block_id(p, bt, kb + BN, U.c1, lane);
+                    uint64_t* full = which ? &v_full[st] : &k_full[st];
+                    uint64_t* empty = which ? &v_empty[st] : &k_empty[st];
+                    if (n > 0 && !mbar_wait_warp(empty, (n - 1) & 1, p.err)) {
+                        s_abort = 1;
+                        ok = false;
+                        continue;
+                    }
+                    uint8_t* dst = smem + (which ? C::kOffV + st * C::kVBytes : C::kOffK + st * C::kKBytes);
+                    if (U.slot == 0) {
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(full, (uint32_t)(nchunk * C::kChunkBytes));
+                            for (int c = 0; c < nchunk; ++c)
+                                tma_load_3d(dst + c * C::kChunkBytes, which ? &maps.vnew : &maps.knew, full, c * 64, U.g,
+                                            U.q0 + kb, pol_kv);
+                        }
+                    } else if (ctx_tma) {
+                        // one lane per block issues that block's boxes (in parallel)
+                        const int bs = p.bs;
+                        const int nvalid = min(BN / bs, (U.c1 - kb + bs - 1) / bs);
+                        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nvalid * nchunk * bs * 128));
+                        __syncwarp();
+                        if (lane < nvalid) {
+                            const int row = (blk_mine * p.Hkv + U.g) * bs;
+                            for (int c = 0; c < nchunk; ++c)
+                                tma_load_2d(dst + c * C::kChunkBytes + lane * bs * 128, which ? &maps.vc : &maps.kc, full,
+                                            c * 64, row, pol_kv);
+                        }
+                    } else {
+                        // small blocks: 16-byte copies, rows past the chunk end zero-filled
+                        const uint32_t dbase = smem_u32(dst);
+                        const __nv_bfloat16* src_base = which ? p.v_cache : p.k_cache;
+                        for (int ci = lane; ci < BN * (width / 8); ci += 32) {
+                            const int row = ci / (width / 8), c = ci % (width / 8);
+                            const int pos = kb + row;
+                            const bool valid = pos < U.c1;
+                            int blk = valid ? __ldg(bt + pos / p.bs) : 0;
+                            if (blk < 0 || blk >= p.num_blocks) {
+                                set_error(p.err, PKA_DEVERR_BLOCK_ID);
+                                blk = 0;
+                            }
+                            const int64_t grow = ((int64_t)blk * p.Hkv + U.g) * p.bs + (valid ? pos % p.bs : 0);
+                            cp_async_16_zfill(dbase + (c >> 3) * C::kChunkBytes + sw128(row, c & 7),
+                                              src_base + grow * width + c * 8, valid);
+                        }
+                        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(full)) : "memory");
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(full);
+                    }
+                    last[st] = n + 1;
+                }
+                if (!ok) break;
             }
-            if (!ok) s_abort = 1;
-            for (int k = 0; k < 2; ++k)
-                if (nq[k] > 0) mbar_wait(&s_full[k], (nq[k] - 1) & 1, p.err);
-        } else if (lane == 0 && warp == 3) {
-            constexpr uint32_t idesc_pv = umma_idesc_bf16(128, DV, 0, 1);
-            const uint32_t v_s = sm_base + C::kOffV;
-            uint32_t kv_it = 0;
-            uint32_t np[2] = {0, 0};  // products issued from P_k
-            uint32_t uo[2] = {0, 0};  // earlier units in which warpgroup k had rows (one epilogue each)
-            bool ok = true;
-            FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
-            for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x) {
-                const FaUnit U = Un;
-                if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
-                for (int t = 0; t < U.nkv; ++t, ++kv_it) {
-                    const int vs = (int)(kv_it % C::kVStages);
-                    if (!mbar_wait(&v_full[vs], (kv_it / C::kVStages) & 1, p.err)) { ok = false; break; }
-                    for (int k = 0; k < 2; ++k) {
-                        if (t >= U.ntk[k]) continue;
-                        if (k == 1 && !wait_counter(s_qk0_next, (int)kv_it + 1, p.err)) { ok = false; break; }
-                        // keys 0..63 of P may be stored before the rest (the softmax's
-                        // one-pass tiles signal them early): their half of the product
-                        // goes first
-                        for (int hh = 0; hh < 2 && ok; ++hh) {
-                            if (!mbar_wait(hh ? &p_full[k] : &p_half[k], np[k] & 1, p.err)) { ok = false; break; }
-                            // a unit's first product overwrites O_k: its previous epilogue must have read it
-                            if (hh == 0 && t == 0 && uo[k] > 0 && !mbar_wait(&o_free[k], (uo[k] - 1) & 1, p.err)) {
-                                ok = false;
-                                break;
-                            }
+            // no copy may outlive the CTA: wait (bounded) for the last one per stage
+            for (int st = 0; st < (which ? C::kVStages : 2); ++st)
+                if (last[st]) mbar_wait_warp(which ? &v_full[st] : &k_full[st], (last[st] - 1) & 1, p.err);
+            if (which == 1 && q_it > 0) mbar_wait_warp(q_full, (q_it - 1) & 1, p.err);
+        } else {  // warps 1 and 3
+            // ------------------------------------------------------------ MMA issuers
+            // warp 1 issues S_k = Q_k K^T for both query tiles of every K tile, each
+            // once the previous P_k . V (which read P_k out of S_k's columns) is
+            // done; warp 3 issues O_k += P_k V as each P_k lands. Each thread
+            // commits only its own MMAs.
+            if (lane == 0 && warp == 1) {
+                constexpr uint32_t idesc_qk = umma_idesc_bf16(128, 128, 0, 0);
+                const uint32_t q_s = sm_base + C::kOffQ, k_s = sm_base + C::kOffK;
+                uint32_t kv_it = 0, q_it = 0;
+                uint32_t nq[2] = {0, 0};  // products issued into S_k
+                bool ok = true;
+                FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
+                for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x, ++q_it) {
+                    const FaUnit U = Un;
+                    if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
+                    if (!mbar_wait(q_full, q_it & 1, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int t = 0; t < U.nkv; ++t, ++kv_it) {
+                        const int st = kv_it & 1;
+                        if (!mbar_wait(&k_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                        // query tile 0 has no S of this tile: tile 1's product of the
+                        // previous tile may go now (its next S below waits for it)
+                        if (t > 0 && t >= U.ntk[0]) s_qk0_next = (int)kv_it;
+                        for (int k = 0; k < 2; ++k) {
+                            if (t >= U.ntk[k]) continue;
+                            if (nq[k] > 0 && !mbar_wait(&pv_done[k], (nq[k] - 1) & 1, p.err)) { ok = false; break; }
                             tc_fence_after();
-#pragma unroll
-                            for (int kq = 0; kq < BN / 32; ++kq) {
-                                const int kk = hh * (BN / 32) + kq;
-                                const uint64_t bdesc =
-                                    umma_desc_sw128(v_s + vs * C::kVBytes + kk * 2048, C::kChunkBytes, 1024);
-                                umma_bf16_ts(tbase + C::kColO + k * DV, tbase + C::kColS + k * 128 + kk * 8, bdesc,
-                                             idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+    #pragma unroll
+                            for (int ks = 0; ks < D / 16; ++ks) {
+                                const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+                                umma_bf16(tbase + C::kColS + k * 128,
+                                          umma_desc_sw128(q_s + k * C::kQBytes + off, 16, 1024),
+                                          umma_desc_sw128(k_s + st * C::kKBytes + off, 16, 1024), idesc_qk,
+                                          ks > 0 ? 1u : 0u);
                             }
+                            umma_commit(&s_full[k]);
+                            ++nq[k];
+                            // query tile 0's S of this tile is issued: query tile 1's
+                            // product of the previous tile may go
+                            if (k == 0 && t > 0) s_qk0_next = (int)kv_it;
                         }
                         if (!ok) break;
-                        umma_commit(&pv_done[k]);
-                        ++np[k];
+                        umma_commit(&k_empty[st]);
+                        if (t == U.nkv - 1) umma_commit(q_empty);
                     }
-                    if (!ok) break;
-                    umma_commit(&v_empty[vs]);
+                    if (ok) s_qk0_next = (int)kv_it;  // the unit's last tile: nothing of query tile 0 follows
                 }
+                if (!ok) s_abort = 1;
                 for (int k = 0; k < 2; ++k)
-                    if (U.ntk[k] > 0) ++uo[k];
+                    if (nq[k] > 0) mbar_wait(&s_full[k], (nq[k] - 1) & 1, p.err);
+            } else if (lane == 0 && warp == 3) {
+                constexpr uint32_t idesc_pv = umma_idesc_bf16(128, DV, 0, 1);
+                const uint32_t v_s = sm_base + C::kOffV;
+                uint32_t kv_it = 0;
+                uint32_t np[2] = {0, 0};  // products issued from P_k
+                uint32_t uo[2] = {0, 0};  // earlier units in which warpgroup k had rows (one epilogue each)
+                bool ok = true;
+                FaUnit Un = blockIdx.x < num_units ? fa_unit(p, blockIdx.x) : FaUnit{};
+                for (int u = blockIdx.x; u < num_units && ok && !s_abort; u += gridDim.x) {
+                    const FaUnit U = Un;
+                    if (u + (int)gridDim.x < num_units) Un = fa_unit(p, u + gridDim.x);
+                    for (int t = 0; t < U.nkv; ++t, ++kv_it) {
+                        const int vs = (int)(kv_it % C::kVStages);
+                        if (!mbar_wait(&v_full[vs], (kv_it / C::kVStages) & 1, p.err)) { ok = false; break; }
+                        for (int k = 0; k < 2; ++k) {
+                            if (t >= U.ntk[k]) continue;
+                            if (k == 1 && !wait_counter(s_qk0_next, (int)kv_it + 1, p.err)) { ok = false; break; }
+                            // keys 0..63 of P may be stored before the rest (the softmax's
+                            // one-pass tiles signal them early): their half of the product
+                            // goes first
+                            for (int hh = 0; hh < 2 && ok; ++hh) {
+                                if (!mbar_wait(hh ? &p_full[k] : &p_half[k], np[k] & 1, p.err)) { ok = false; break; }
+                                // a unit's first product overwrites O_k: its previous epilogue must have read it
+                                if (hh == 0 && t == 0 && uo[k] > 0 && !mbar_wait(&o_free[k], (uo[k] - 1) & 1, p.err)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+    #pragma unroll
+                                for (int kq = 0; kq < BN / 32; ++kq) {
+                                    const int kk = hh * (BN / 32) + kq;
+                                    const uint64_t bdesc =
+                                        umma_desc_sw128(v_s + vs * C::kVBytes + kk * 2048, C::kChunkBytes, 1024);
+                                    umma_bf16_ts(tbase + C::kColO + k * DV, tbase + C::kColS + k * 128 + kk * 8, bdesc,
+                                                 idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                                }
+                            }
+                            if (!ok) break;
+                            umma_commit(&pv_done[k]);
+                            ++np[k];
+                        }
+                        if (!ok) break;
+                        umma_commit(&v_empty[vs]);
+                    }
+                    for (int k = 0; k < 2; ++k)
+                        if (U.ntk[k] > 0) ++uo[k];
+                }
+                if (!ok) s_abort = 1;
+                // let every issued MMA finish before the CTA can exit
+                for (int k = 0; k < 2; ++k)
+                    if (np[k] > 0) mbar_wait(&pv_done[k], (np[k] - 1) & 1, p.err);
             }
-            if (!ok) s_abort = 1;
-            // let every issued MMA finish before the CTA can exit
-            for (int k = 0; k < 2; ++k)
-                if (np[k] > 0) mbar_wait(&pv_done[k], (np[k] - 1) & 1, p.err);
         }
-    } else if (warp >= 4) {
+    } else {
+        setmaxnreg_inc<kFaRegsSoftmax>();
         // ------------------------------------------------------------ softmax warpgroups
         const int k = warp >= 8 ? 1 : 0;        // this warpgroup's query tile
         const int row = 32 * (warp & 3) + lane;  // TMEM lane = query row of the tile
@@ -425,10 +434,10 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                 const bool edge = (U.slot == 0) ? (kb + BN - 1 > row0 || kb + BN > c1) : (kb < U.c0 || kb + BN > c1);
                 const int lo = U.c0 - kb;  // visible columns: [lo, hi)
                 const int hi = ((U.slot == 0) ? min(qi + 1, c1) : c1) - kb;
-                // General body, two passes over S_k in TMEM. Pass 1: row max of the
-                // raw scores (8 independent chains). Pass 2: P = exp2(scale * s -
-                // m_used) as bf16 pairs, written over S_k's already-read columns
-                // (keys 64h.. land in columns 32h..). Specialised on whether the
+                // General body, two passes over the row of S_k (held in registers).
+                // Pass 1: row max of the raw scores (8 independent chains). Pass 2:
+                // P = exp2(scale * s - m_used) as bf16 pairs, written over S_k's
+                // already-read columns (keys 64h.. land in columns 32h..). Specialised on whether the
                 // tile needs a mask at all (a per-element mask costs ALU issue
                 // slots on every tile otherwise).
                 float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -471,17 +480,19 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                                  fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
                 };
                 auto tile_body = [&](auto masked_c) {
+                    // the whole row of S_k in one TMEM round trip, kept in registers
+                    // for both passes
+                    uint32_t r0[64], r1[64];
+                    tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(r0));
+                    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(r0 + 32));
+                    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(r1));
+                    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(r1 + 32));
+                    tmem_wait_ld();
                     float mxv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) mxv[j] = -INFINITY;
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {  // 64 columns per TMEM round trip
-                        uint32_t r[64];
-                        tmem_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(r));
-                        tmem_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-                        tmem_wait_ld();
-                        max_half(r, mxv, masked_c, h);
-                    }
+                    max_half(r0, mxv, masked_c, 0);
+                    max_half(r1, mxv, masked_c, 1);
                     const float m_new = fmaxf(m_used, reduce8(mxv) * sl2);
                     if (t == 0) {
                         m_used = m_new;
@@ -492,57 +503,44 @@ __global__ void __launch_bounds__(kFaThreads, 1) fa_fwd_kernel(const __grid_cons
                         m_used = m_new;
                     }
                     const float m_off = m_used == -INFINITY ? 0.f : m_used;
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {  // 64 columns per TMEM round trip
-                        uint32_t r[64];
-                        tmem_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(r));
-                        tmem_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-                        tmem_wait_ld();
-                        uint32_t pk[32];
-                        exp_half(r, pk, m_off, masked_c, h);
-                        // keys 64h.. land in P columns 32h.. (S columns already read)
-                        tmem_st32(tS + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-                    }
+                    uint32_t pk[32];
+                    // keys 64h.. land in P columns 32h.. (S columns already read)
+                    exp_half(r0, pk, m_off, masked_c, 0);
+                    tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                    exp_half(r1, pk, m_off, masked_c, 1);
+                    tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk));
                 };
                 // Common case, one pass: an unmasked tile after the row's first,
                 // whose scores stay within the lazy-rescale margin of m_used, gets
-                // its exponentials as each half is read. Half 0's P stays in
-                // registers until half 1's max is known, so S_k is intact in TMEM
-                // when a row of the warp turns out to need more (then the general
-                // body runs from the start; the choice is warp-uniform because
+                // its exponentials straight after the row max. When a row of the
+                // warp needs more, nothing has been written yet and the general
+                // body runs from the start (the choice is warp-uniform because
                 // tcgen05.ld/st are warp-collective).
                 auto tile_fast = [&]() -> bool {
-                    uint32_t pk0[32];
-                    {
-                        uint32_t r[64];
-                        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(r));
-                        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-                        tmem_wait_ld();
-                        float mxv[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) mxv[j] = -INFINITY;
-                        max_half(r, mxv, std::false_type{}, 0);
-                        if (__any_sync(0xffffffffu, reduce8(mxv) * sl2 > m_used + 8.f)) return false;
-                        exp_half(r, pk0, m_used, std::false_type{}, 0);
-                    }
-                    uint32_t r[64];
-                    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(r));
-                    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                    // both halves of S_k come in one TMEM round trip (the softmax
+                    // warpgroups have the registers for it)
+                    uint32_t r0[64], r1[64];
+                    tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(r0));
+                    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(r0 + 32));
+                    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(r1));
+                    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(r1 + 32));
                     tmem_wait_ld();
                     float mxv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) mxv[j] = -INFINITY;
-                    max_half(r, mxv, std::false_type{}, 1);
+                    max_half(r0, mxv, std::false_type{}, 0);
+                    max_half(r1, mxv, std::false_type{}, 1);
                     if (__any_sync(0xffffffffu, reduce8(mxv) * sl2 > m_used + 8.f)) return false;
-                    tmem_st32(tS, pk0);  // keys 0..63 -> P columns 0..31 (S columns 0..63 were read)
+                    uint32_t pk[32];
+                    exp_half(r0, pk, m_used, std::false_type{}, 0);
+                    tmem_st32(tS, pk);  // keys 0..63 -> P columns 0..31 (S columns 0..127 were read)
                     // their half of P . V may start while the rest is computed (no
-                    // rescale on this path, and no V rows to zero: both need a mask)
+                    // rescale on this path, and no value rows to zero: both need a mask)
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&p_half[k]);
-                    uint32_t pk[32];
-                    exp_half(r, pk, m_used, std::false_type{}, 1);
+                    exp_half(r1, pk, m_used, std::false_type{}, 1);
                     tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk));
                     return true;
                 };
