@@ -259,6 +259,45 @@ PKA_API pka_status pka_paged_attn_forward_fp8(const void *q, const void *k_new, 
                                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pka_paged_attn_step / pka_paged_attn_step_fp8 -- one whole serving step:
+ * the cache write of the new tokens (pka_cache_write / pka_cache_write_fp8
+ * with k_new, v_new and slot_mapping) followed by the forward pass
+ * (pka_paged_attn_forward / _fp8), as the pages' unified forward() runs its
+ * stage 1 "save key/value into the KV cache" before the attention ("Beyond
+ * porting", unified backends). Same results as the two calls in a row; in one
+ * call the planner, which reads no cache, runs while the cache write runs
+ * (and waits for it before the kernels that read the cache start).
+ *
+ *   slot_mapping       device int64 [num_tokens], as in pka_cache_write (not NULL)
+ *   k_new, v_new       required (v_new NULL with a latent cache, v_cache NULL)
+ *   cache_error_word   device int32, or NULL: the cache write's error bits
+ *                      (PKA_DEVERR_SLOT), or-ed in; the caller clears it
+ *   k_cache, v_cache   written (the new tokens' slots), then read
+ * Every other argument, the workspace (pka_workspace_size / _fp8) and the
+ * supported shapes are those of the forward call; validation failures return
+ * before any launch.
+ */
+PKA_API pka_status pka_paged_attn_step(const void *q, const void *k_new, const void *v_new,
+                                       const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                       const int32_t *block_table, int max_blocks_per_req,
+                                       const int32_t *query_start_loc, const int32_t *seq_lens, int num_decodes,
+                                       int num_extends, int num_prefills, int num_tokens, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int head_dim_v, int64_t num_blocks,
+                                       int block_size, float scale, int context_chunk_tokens, int max_query_len,
+                                       int max_seq_len, void *out, float *lse, int32_t *cache_error_word,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+PKA_API pka_status pka_paged_attn_step_fp8(const void *q, const void *k_new, const void *v_new,
+                                           const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                           const int32_t *block_table, int max_blocks_per_req,
+                                           const int32_t *query_start_loc, const int32_t *seq_lens,
+                                           int num_decodes, int num_extends, int num_prefills, int num_tokens,
+                                           int num_q_heads, int num_kv_heads, int head_dim, int head_dim_v,
+                                           int64_t num_blocks, int block_size, float scale, float k_scale,
+                                           float v_scale, int context_chunk_tokens, int max_query_len,
+                                           int max_seq_len, void *out, float *lse, int32_t *cache_error_word,
+                                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * pka_merge_attn_states -- combine two partial attention results over
  * disjoint key sets (the pages' merge_attn_states, extend path):
  *     m = max(la, lb), wa = exp(la - m), wb = exp(lb - m)

@@ -434,7 +434,8 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
                         int num_prefills, int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
                         int head_dim_v, int64_t num_blocks, int block_size, float scale, int context_chunk_tokens,
                         int max_query_len, int max_seq_len, void* out, float* lse, void* workspace,
-                        size_t workspace_bytes, void* stream, const CacheFormat& cf) {
+                        size_t workspace_bytes, void* stream, const CacheFormat& cf,
+                        const int64_t* slot_mapping = nullptr, int32_t* cache_error_word = nullptr) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int B = num_decodes + num_extends + num_prefills;
     if (B == 0 && num_tokens == 0) return PKA_OK;
@@ -462,6 +463,12 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
     if (max_blocks_per_req <= 0 || num_blocks <= 0 || !pow2(block_size) || block_size > 128)
         return block_size > 128 || !pow2(block_size) ? PKA_ERR_UNSUPPORTED : PKA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return PKA_ERR_INVALID_ARG;  // masking and the row max assume scale > 0
+    const bool fused_write = slot_mapping != nullptr && num_tokens > 0;
+    if (fused_write) {  // the step's own cache write: the new tokens' K/V into their slots
+        if (!k_new || (v_cache != nullptr) != (v_new != nullptr)) return PKA_ERR_INVALID_ARG;
+        if (!aligned(slot_mapping, 8) || (cache_error_word && !aligned(cache_error_word, 4))) return PKA_ERR_INVALID_ARG;
+        if (head_dim % 8 != 0 || head_dim_v % 8 != 0) return PKA_ERR_UNSUPPORTED;
+    }
     const int64_t cache_rows = num_blocks * num_kv_heads * (int64_t)block_size;
     if (cache_rows >= (int64_t)INT32_MAX) return PKA_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_req * block_size < max_seq_len) return PKA_ERR_INVALID_ARG;
@@ -506,6 +513,18 @@ pka_status forward_impl(const void* q, const void* k_new, const void* v_new, con
     pp.dec_nsplit = reinterpret_cast<int32_t*>(ws + L.off_dec_nsplit);
     pp.fa_items = reinterpret_cast<int4*>(ws + L.off_fa_items);
     pp.ext_base = reinterpret_cast<int32_t*>(ws + L.off_ext_base);
+    pp.after_cache_write = fused_write ? 1 : 0;
+    if (fused_write) {
+        // launched first; the planner, which reads no cache, overlaps it and
+        // waits for it before the kernels that read the cache may start
+        if ((e = timed(PKA_KERNEL_CACHE_WRITE, st, [&] {
+                 return launch_cache_write(k_new, v_new, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                           is_mla ? 0 : head_dim_v, const_cast<void*>(k_cache),
+                                           const_cast<void*>(v_cache), num_blocks, block_size, cache_error_word, sms,
+                                           st, cf.fp8, cf.k_scale, cf.v_scale);
+             })) != cudaSuccess)
+            return PKA_ERR_CUDA;
+    }
     if ((e = timed(PKA_KERNEL_PLANNER, st, [&] { return launch_planner(pp, st); })) != cudaSuccess)
         return PKA_ERR_CUDA;
 
@@ -755,6 +774,38 @@ pka_status pka_paged_attn_forward_fp8(const void* q, const void* k_new, const vo
                         head_dim, head_dim_v, num_blocks, block_size, scale, context_chunk_tokens, max_query_len,
                         max_seq_len, out, lse, workspace, workspace_bytes, stream,
                         CacheFormat{true, k_scale, v_scale});
+}
+
+pka_status pka_paged_attn_step(const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                               void* k_cache, void* v_cache, const int32_t* block_table, int max_blocks_per_req,
+                               const int32_t* query_start_loc, const int32_t* seq_lens, int num_decodes,
+                               int num_extends, int num_prefills, int num_tokens, int num_q_heads, int num_kv_heads,
+                               int head_dim, int head_dim_v, int64_t num_blocks, int block_size, float scale,
+                               int context_chunk_tokens, int max_query_len, int max_seq_len, void* out, float* lse,
+                               int32_t* cache_error_word, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!slot_mapping) return PKA_ERR_INVALID_ARG;
+    return forward_impl(q, k_new, v_new, k_cache, v_cache, block_table, max_blocks_per_req, query_start_loc,
+                        seq_lens, num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads,
+                        head_dim, head_dim_v, num_blocks, block_size, scale, context_chunk_tokens, max_query_len,
+                        max_seq_len, out, lse, workspace, workspace_bytes, stream, CacheFormat{false, 1.f, 1.f},
+                        slot_mapping, cache_error_word);
+}
+
+pka_status pka_paged_attn_step_fp8(const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                   void* k_cache, void* v_cache, const int32_t* block_table, int max_blocks_per_req,
+                                   const int32_t* query_start_loc, const int32_t* seq_lens, int num_decodes,
+                                   int num_extends, int num_prefills, int num_tokens, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int head_dim_v, int64_t num_blocks,
+                                   int block_size, float scale, float k_scale, float v_scale,
+                                   int context_chunk_tokens, int max_query_len, int max_seq_len, void* out,
+                                   float* lse, int32_t* cache_error_word, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    if (!slot_mapping) return PKA_ERR_INVALID_ARG;
+    return forward_impl(q, k_new, v_new, k_cache, v_cache, block_table, max_blocks_per_req, query_start_loc,
+                        seq_lens, num_decodes, num_extends, num_prefills, num_tokens, num_q_heads, num_kv_heads,
+                        head_dim, head_dim_v, num_blocks, block_size, scale, context_chunk_tokens, max_query_len,
+                        max_seq_len, out, lse, workspace, workspace_bytes, stream, CacheFormat{true, k_scale, v_scale},
+                        slot_mapping, cache_error_word);
 }
 
 pka_status pka_merge_attn_states(void* out, float* out_lse, const void* prefix_out, const float* prefix_lse,

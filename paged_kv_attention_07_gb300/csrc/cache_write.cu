@@ -70,6 +70,8 @@ template <bool kFp8, int kCwPieces, bool kWide>
 __global__ void __launch_bounds__(256) cache_write_kernel(CacheWriteParams p) {
     using Idx = typename std::conditional<kWide, int64_t, uint32_t>::type;
     constexpr int kRows = cw_rows<kCwPieces>();
+    // a forward step's planner may start now: it reads no cache
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const Idx warp = (Idx)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const Idx rows = (Idx)(p.num_tokens * p.num_kv_heads);

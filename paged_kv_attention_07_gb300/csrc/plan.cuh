@@ -63,6 +63,11 @@ struct PlanParams {
     int32_t* dec_first;
     int32_t* dec_nsplit;
     int4* fa_items;      // (request, pair of query tiles, slot, cost)
+    // 1: the kernel before this one is the same call's cache write, launched
+    // to let the planner start at once (the planner reads no cache). The
+    // planner then waits for it before finishing, so the kernels that depend
+    // on the plan also see the written cache.
+    int after_cache_write;
     int32_t* ext_base;   // per extend request: first partial row
 };
 

@@ -56,7 +56,7 @@ __device__ int scan_ranges(int n, int32_t* scan, CountF count, EmitF emit) {
     return total;
 }
 
-__global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
+__device__ __forceinline__ void plan_body(const PlanParams& p) {
     __shared__ int32_t s_qlen[kMaxRequests];
     __shared__ int32_t s_slen[kMaxRequests];
     __shared__ int32_t s_hist[kCostBuckets];
@@ -242,7 +242,13 @@ __global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
     }
 }
 
+__global__ void __launch_bounds__(1024) planner_kernel(PlanParams p) {
+    plan_body(p);
+    if (p.after_cache_write) grid_dep_wait();  // finish only after the cache write
+}
+
 cudaError_t launch_planner(const PlanParams& p, cudaStream_t stream) {
+    if (p.after_cache_write) return launch_dependent(planner_kernel, dim3(1), dim3(1024), 0, stream, p);
     planner_kernel<<<1, 1024, 0, stream>>>(p);
     return cudaGetLastError();
 }

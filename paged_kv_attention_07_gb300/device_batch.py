@@ -221,6 +221,16 @@ class DeviceBatch:
                                    head_dim_v=s.head_dim_v, stream=stream)
 
     def step(self, stream=None):
+        """The whole step in one call: the new tokens' cache write, then the
+        forward pass (pka_paged_attn_step)."""
+        s = self.spec
+        pka.pka_paged_attn_step(self.q, self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                                self.block_table, self.qsl, self.seq_lens, *self.counts, s.scale, s.context_chunk,
+                                self.max_query_len, self.max_seq_len, self.out, self.lse, self.workspace,
+                                kv_scales=self.kv_scales, stream=stream)
+
+    def step_separate(self, stream=None):
+        """The same step as two calls: pka_cache_write(_fp8), then the forward."""
         self.cache_write(stream)
         self.forward(stream)
 

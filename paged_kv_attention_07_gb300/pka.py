@@ -21,7 +21,7 @@ DEVERR = {"QUERY_START_LOC": 0x01, "SEQ_LEN": 0x02, "ORDER": 0x04, "QUERY_LEN": 
           "INDEX": 0x200}
 EXPORTED = ("pka_cache_write", "pka_cache_write_fp8", "pka_workspace_size", "pka_workspace_size_fp8",
             "pka_paged_attn_forward",
-            "pka_paged_attn_forward_fp8",
+            "pka_paged_attn_forward_fp8", "pka_paged_attn_step", "pka_paged_attn_step_fp8",
             "pka_merge_attn_states", "pka_get_error", "pka_paged_decode_noalloc", "pka_kernel_timer",
             "pka_kernel_timer_read", "pka_batch_order", "pka_gather_rows", "pka_selftest_wait",
             "pka_status_string")
@@ -60,6 +60,15 @@ def load(path: str | None = None):
     lib.pka_paged_attn_forward_fp8.restype = i32
     lib.pka_paged_attn_forward_fp8.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
                                                i32, i32, i64, i32, f32, f32, f32, i32, i32, i32, P, P, P, sz, P]
+    # q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, max_blocks, qsl, seq_lens, nd, ne, np, T,
+    # Hq, Hkv, d, dv, num_blocks, bs, scale, [k_scale, v_scale,] chunk, max_q, max_s, out, lse, cw_err, ws,
+    # ws_bytes, stream
+    lib.pka_paged_attn_step.restype = i32
+    lib.pka_paged_attn_step.argtypes = [P, P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                        i64, i32, f32, i32, i32, i32, P, P, P, P, sz, P]
+    lib.pka_paged_attn_step_fp8.restype = i32
+    lib.pka_paged_attn_step_fp8.argtypes = [P, P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                            i64, i32, f32, f32, f32, i32, i32, i32, P, P, P, P, sz, P]
     lib.pka_workspace_size.restype = sz
     lib.pka_workspace_size.argtypes = [i32] * 11
     lib.pka_workspace_size_fp8.restype = sz
@@ -179,6 +188,26 @@ def pka_paged_attn_forward_fp8(q, k_new, v_new, k_cache, v_cache, block_table, q
         context_chunk_tokens, max_query_len, max_seq_len, _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "pka_paged_attn_forward_fp8")
+
+
+def pka_paged_attn_step(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, query_start_loc, seq_lens,
+                        num_decodes, num_extends, num_prefills, scale, context_chunk_tokens, max_query_len,
+                        max_seq_len, out, lse, workspace, error_word=None, kv_scales=None, stream=None):
+    """Cache write of the new tokens + forward pass in one call (bf16 cache, or
+    an 8-bit cache with kv_scales=(k_scale, v_scale))."""
+    T, Hq, d = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    dv = out.shape[2]
+    common = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+              block_table.shape[1], _ptr(query_start_loc), _ptr(seq_lens), num_decodes, num_extends, num_prefills,
+              T, Hq, Hkv, d, dv, nb, bs, float(scale))
+    tail = (context_chunk_tokens, max_query_len, max_seq_len, _ptr(out), _ptr(lse), _ptr(error_word),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if kv_scales is None:
+        st = load().pka_paged_attn_step(*common, *tail)
+    else:
+        st = load().pka_paged_attn_step_fp8(*common, float(kv_scales[0]), float(kv_scales[1]), *tail)
+    _check(st, "pka_paged_attn_step")
 
 
 def pka_merge_attn_states(out, out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse, stream=None):

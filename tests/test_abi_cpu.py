@@ -140,3 +140,12 @@ def test_fp8_entry_points_reject_bad_arguments(lib):
     assert lib.pka_workspace_size_fp8(1, 1, 1, 8, 8, 2, 64, 64, 6, 100, 32) == 0
     assert lib.pka_workspace_size_fp8(1, 1, 1, 8, 8, 2, 192, 128, 6, 100, 32) == 0
     assert fwd(ks=0.0) == 1 and fwd(vs=float("inf")) == 1
+
+
+def test_step_entry_points_reject_bad_arguments(lib):
+    # no slot mapping: the step's cache write has nothing to write with
+    for fn, extra in ((lib.pka_paged_attn_step, ()), (lib.pka_paged_attn_step_fp8,
+                                                       (ctypes.c_float(0.5), ctypes.c_float(0.5)))):
+        args = [FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 8, FAKE, FAKE, 2, 0, 0, 2, 8, 2, 128, 128, 64, 16,
+                ctypes.c_float(0.125), *extra, 32, 1, 100, FAKE, None, None, P(0x100000), 1 << 20, None]
+        assert fn(*args) == 1

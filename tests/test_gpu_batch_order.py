@@ -152,3 +152,44 @@ def test_packed_staging_buffers_give_the_same_step():
     lse = host_out[lse_off:lse_off + T * Hq * 4].view(torch.float32).numpy().reshape(-1)
     ref_o, ref_l = oracle.batch_reference(batch)
     assert np.abs(out - ref_o).max() <= OUT_ATOL and np.abs(lse - ref_l).max() <= LSE_ATOL
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8", "mla"])
+def test_one_call_step_equals_two_calls(kind):
+    """pka_paged_attn_step (cache write and forward in one call, the planner
+    overlapping the write) gives the cache, out and lse of pka_cache_write
+    followed by the forward call, bit for bit."""
+    if kind == "mla":
+        spec = W.spec_custom("step_mla", ctx=[100, 900, 64], qlen=[1, 1, 1], num_decodes=3, num_extends=0,
+                             num_prefills=0, Hq=128, Hkv=1, d=576, dv=512, bs=64, scale=1 / np.sqrt(192),
+                             mla=True, seed=81)
+    else:
+        spec = W.spec_custom("step_" + kind, ctx=[40, 300, 70, 0], qlen=[1, 1, 30, 50], num_decodes=2,
+                             num_extends=1, num_prefills=1, Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=64, seed=82)
+    batch = W.make_batch(spec)
+    scales = (0.0125, 0.02) if kind == "fp8" else None
+    a, b = DeviceBatch(batch, kv_scales=scales), DeviceBatch(batch, kv_scales=scales)
+    a.step()
+    b.step_separate()
+    torch.cuda.synchronize()
+    assert a.error_word() == 0 and b.error_word() == 0 and a.canaries_intact()
+    bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t  # unwritten slots hold NaN
+    assert torch.equal(bits(a.k_cache), bits(b.k_cache))
+    if a.v_cache is not None:
+        assert torch.equal(bits(a.v_cache), bits(b.v_cache))
+    assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
+
+
+def test_one_call_step_reports_a_bad_slot():
+    spec = W.spec_custom("step_bad", ctx=[40, 70], qlen=[1, 30], num_decodes=1, num_extends=1, num_prefills=0,
+                         Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=64, seed=83)
+    db = DeviceBatch(W.make_batch(spec))
+    db.slot_mapping[3] = db.k_cache.shape[0] * spec.block_size + 5  # past the cache
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = spec
+    pka.pka_paged_attn_step(db.q, db.k_new, db.v_new, db.slot_mapping, db.k_cache, db.v_cache, db.block_table,
+                            db.qsl, db.seq_lens, *db.counts, s.scale, s.context_chunk, db.max_query_len,
+                            db.max_seq_len, db.out, db.lse, db.workspace, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pka.DEVERR["SLOT"]
+    assert db.canaries_intact()
