@@ -286,7 +286,7 @@ def secondary_workloads(device, steps, warmup, peaks, rank):
              ("prefill_varlen", W.spec_prefill(), "prefill_extend", "tensor", 256 << 20,
               ("fa_fwd.cu", "fa_fwd_prefill_varlen")),
              ("mixed", W.spec_mixed(), "prefill_extend", "tensor", 0, ("fa_fwd.cu", "fa_fwd_mixed")),
-             ("mixed_fp8", W.spec_mixed(), "prefill_extend", "tensor", 0, None),
+             ("mixed_fp8", W.spec_mixed(), "prefill_extend", "tensor", 0, ("fa_fwd.cu", "fa_fwd_mixed_fp8")),
              ("mla_prefill_extend", W.spec_mla_prefill(), "prefill_extend", "tensor", 0,
               ("fa_fwd.cu", "fa_fwd_mla_prefill_extend")),
              ("mla_decode_bs64", W.spec_mla_decode(), "decode", "hbm", 0,
