@@ -14,12 +14,16 @@
 // in the unit order, so the second read of every latent tile hits L2.
 //
 // Tensor memory (512 columns, lane = head):
-//     [0, 64)    S   fp32 scores of a 64-key tile
-//     [64, 96)   P   bf16 pairs, the A operand of O += P . V
-//     [96, 256)  Qt  bf16 pairs of q[:, 0:320], the A operand of the first
-//                    20 k-steps of S (no shared-memory traffic for them)
+//     [0, 128)   S   two buffers of fp32 scores of a 64-key tile; the
+//                    softmax writes that tile's P (bf16 pairs, the A operand
+//                    of O += P . V) over the first 32 columns of its buffer
+//     [128, 256) Qt  bf16 pairs of q[:, 0:256], the A operand of the first
+//                    16 k-steps of S (no shared-memory traffic for them)
 //     [256, 512) O   fp32, this unit's 256 value dims
-// Shared memory: q[:, 320:576] (64 KB, the A operand of the last 16 k-steps)
+// With two S buffers the scores of the next tile are issued right after the
+// current tile's, while the softmax works on the current one: a buffer is
+// reused once the P . V that read its P has completed.
+// Shared memory: q[:, 256:576] (80 KB, the A operand of the last 20 k-steps)
 // and a 2-stage ring of 64-key latent tiles (72 KB each), loaded with TMA
 // boxes of 64 dims x min(block size, 64) rows walked through the block table;
 // below block size 8, and for a split's last, partial tile, TMA gathers of
@@ -30,10 +34,13 @@
 // from an atomic counter; warp 0 publishes each unit index to the other roles
 // through a 2-slot ring in shared memory. Warps: 0 producer of q and the
 // score-only chunks, 6 producer of the value chunks, 1 tensor-memory owner +
-// MMA issuer (one thread), 2-5 softmax (one thread per head):
+// MMA issuer (one elected lane issues), 2-5 softmax (one thread per head):
 // S row -> online softmax (the O rescale is lazy: only when the max grew by
 // more than 2^8) -> P into TMEM; at the end of a unit O / l goes to out, or
 // to the fp32 split partials + LSE that the decode reduction merges.
+// Per tile t the issuer runs S(t) part 1, O += P(t-1) . V(t-1), S(t) part 2;
+// the commit after S(t) part 2 thus also covers the P . V before it, so the
+// softmax may rescale O as soon as it sees S(t).
 #include <type_traits>
 
 #include "common.cuh"
@@ -46,16 +53,19 @@ namespace pka {
 constexpr int kMtThreads = 224;
 constexpr int kMtTile = 64;                       // keys per tile (the N of S)
 constexpr int kMtD = 576, kMtDv = 512, kMtHalf = 256;
-constexpr int kMtQtDims = 320;                    // q dims held in TMEM
+constexpr int kMtQtDims = 256;                    // q dims held in TMEM
 constexpr int kMtChunk = kMtTile * 128;           // one 64-dim column chunk of a tile (8 KB)
 constexpr int kMtTileBytes = 9 * kMtChunk;        // 72 KB
 constexpr int kMtQsChunk = 128 * 128;             // 128 heads x 64 dims
-constexpr int kMtQsBytes = 4 * kMtQsChunk;        // q[:, 320:576]
+constexpr int kMtQsChunks = (kMtD - kMtQtDims) / 64;
+constexpr int kMtQsBytes = kMtQsChunks * kMtQsChunk;  // q[:, 256:576]
 constexpr int kMtOffQ = 0;
 constexpr int kMtOffKV = kMtQsBytes;
 constexpr int kMtOffBar = kMtOffKV + 2 * kMtTileBytes;
 constexpr int kMtSmem = kMtOffBar + 256 + 1024;
-constexpr uint32_t kMtColS = 0, kMtColP = 64, kMtColQ = 96, kMtColO = 256, kMtCols = 512;
+constexpr uint32_t kMtColS = 0, kMtColQ = 128, kMtColO = 256, kMtCols = 512;  // S buffer b at kMtColS + 64 b
+static_assert(kMtSmem <= 227 * 1024, "shared memory");
+static_assert(kMtColQ + kMtQtDims / 2 == kMtColO && kMtColS + 2 * kMtTile == kMtColQ, "tensor memory columns");
 
 struct MlaTcUnit {
     int pair, grp, half, r, k0, k1, ntiles;
@@ -97,13 +107,13 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     uint64_t* kv_empty_v = bars + 18; // [2] value chunks read by S and P . V
     uint64_t* u_full = bars + 4;     // [2] unit ring slot written
     uint64_t* u_empty = bars + 6;    // [2] unit ring slot read by the issuer, the value producer and the 4 softmax warps
-    uint64_t* q_full = bars + 8;     // q[:, 320:576] landed in shared memory
+    uint64_t* q_full = bars + 8;     // q[:, 256:576] landed in shared memory
     uint64_t* q_empty = bars + 9;    // the unit's last S product is done (Q free again)
-    uint64_t* qt_ready = bars + 10;  // q[:, 0:320] written to TMEM (4 warps)
-    uint64_t* s_full = bars + 11;
-    uint64_t* s_free = bars + 12;    // 4 warps read S
+    uint64_t* qt_ready = bars + 10;  // q[:, 0:256] written to TMEM (4 warps)
+    uint64_t* s_full = bars + 11;    // a tile's S complete (and the P . V issued before its part 2)
     uint64_t* p_full = bars + 13;    // 4 warps wrote P (and rescaled O)
-    uint64_t* pv_done = bars + 14;
+    uint64_t* pv_buf = bars + 20;    // [2] the P . V reading S buffer b complete: b free again
+    uint64_t* o_full = bars + 22;    // a unit's last P . V complete
     uint64_t* o_free = bars + 15;    // 4 warps read O
     __shared__ uint32_t s_tmem;
     __shared__ int s_unit[2];
@@ -127,9 +137,10 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         mbar_init(q_empty, 1);
         mbar_init(qt_ready, 4);
         mbar_init(s_full, 1);
-        mbar_init(s_free, 4);
         mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
+        mbar_init(&pv_buf[0], 1);
+        mbar_init(&pv_buf[1], 1);
+        mbar_init(o_full, 1);
         mbar_init(o_free, 4);
         fence_barrier_init();
         s_abort = 0;
@@ -156,7 +167,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
 
     if (warp == 0 || warp == 6) {
         // ------------------------------------------------------------ producers
-        // warp 0 takes the units and loads q[:, 320:576] and the score-only
+        // warp 0 takes the units and loads q[:, 256:576] and the score-only
         // part of each stage; warp 6 loads the value part, so neither part of
         // a stage waits behind the other's free slot.
         const int part = warp == 6 ? 1 : 0;
@@ -197,7 +208,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(q_full, kMtQsBytes);
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < kMtQsChunks; ++c)
                         tma_load_3d(smem + kMtOffQ + c * kMtQsChunk, &qmap, q_full, kMtQtDims + c * 64, U.grp * 128,
                                     U.r, pol);
                 }
@@ -278,17 +289,20 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         if (q_it > 0) mbar_wait_warp(q_full, (q_it - 1) & 1, p.err);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // The whole warp runs this loop (waits, counters and descriptors are
+        // warp-uniform) and one elected lane issues each MMA and commit.
         constexpr uint32_t idesc_s = umma_idesc_bf16(128, kMtTile, 0, 0);
         constexpr uint32_t idesc_o = umma_idesc_bf16(128, kMtHalf, 0, 1);
         const uint32_t q_s = sm_base + kMtOffQ, kv_s = sm_base + kMtOffKV;
         uint32_t kv_it = 0, s_it = 0, pv_it = 0, q_it = 0;
+        uint32_t pv_last = 0;  // tile (S counter) of the last P . V issued
         bool ok = true;
         // S = q . C^T over all 576 dims, in two parts: the score-only chunks
         // first (their stage part is released right after), then the value
-        // chunks. k-steps over q[:, 0:320] take A from TMEM, the rest from
+        // chunks. k-steps over q[:, 0:256] take A from TMEM, the rest from
         // shared memory. The chunk sets are fixed per value half, so each part
         // is straight-line code.
-        auto issue_s_part = [&](uint32_t kvi, auto half_c, auto part_c) {
+        auto issue_s_part = [&](uint32_t kvi, uint32_t tS, auto half_c, auto part_c) {
             constexpr int H = decltype(half_c)::value, PART = decltype(part_c)::value;
             constexpr int first_c = H ? 0 : 4;  // first chunk of part 0: it starts the accumulation
             const uint32_t kv = kv_s + (kvi & 1) * kMtTileBytes;
@@ -302,28 +316,29 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                     const uint64_t bdesc = umma_desc_sw128(kv + c * kMtChunk + kk * 32, 16, 1024);
                     const uint32_t acc = (PART == 0 && c == first_c && kk == 0) ? 0u : 1u;
                     if (c < kMtQtDims / 64)
-                        umma_bf16_ts(tbase + kMtColS, tbase + kMtColQ + ks * 8, bdesc, idesc_s, acc);
+                        umma_bf16_ts_w(tS, tbase + kMtColQ + ks * 8, bdesc, idesc_s, acc);
                     else
-                        umma_bf16(tbase + kMtColS,
-                                  umma_desc_sw128(q_s + (c - kMtQtDims / 64) * kMtQsChunk + kk * 32, 16, 1024), bdesc,
-                                  idesc_s, acc);
+                        umma_bf16_w(tS, umma_desc_sw128(q_s + (c - kMtQtDims / 64) * kMtQsChunk + kk * 32, 16, 1024),
+                                    bdesc, idesc_s, acc);
                 }
             }
         };
-        // O(half) += P . C[:, half*256 .. +256)
-        auto issue_o = [&](uint32_t kvi, int half, bool first) -> bool {
-            if (!mbar_wait(p_full, pv_it & 1, p.err)) return false;
+        // O(half) += P . C[:, half*256 .. +256), P in the first 32 columns of
+        // S buffer b; the commit on pv_buf[b] frees that buffer
+        auto issue_o = [&](uint32_t kvi, int half, bool first, uint32_t b) -> bool {
+            if (!mbar_wait_warp(p_full, pv_it & 1, p.err)) return false;
             // a unit's first product overwrites O: the previous unit's O must have been read
-            if (first && q_it > 1 && !mbar_wait(o_free, (q_it - 2) & 1, p.err)) return false;
+            if (first && q_it > 1 && !mbar_wait_warp(o_free, (q_it - 2) & 1, p.err)) return false;
             tc_fence_after();
             const uint32_t v = kv_s + (kvi & 1) * kMtTileBytes + half * 4 * kMtChunk;
 #pragma unroll
             for (int kk = 0; kk < kMtTile / 16; ++kk)
-                umma_bf16_ts(tbase + kMtColO, tbase + kMtColP + kk * 8, umma_desc_sw128(v + kk * 16 * 128, kMtChunk, 1024),
-                             idesc_o, (!first || kk > 0) ? 1u : 0u);
-            umma_commit(pv_done);
-            umma_commit(&kv_empty_v[kvi & 1]);
+                umma_bf16_ts_w(tbase + kMtColO, tbase + kMtColS + b * kMtTile + kk * 8,
+                               umma_desc_sw128(v + kk * 16 * 128, kMtChunk, 1024), idesc_o, (!first || kk > 0) ? 1u : 0u);
+            umma_commit_w(&pv_buf[b]);
+            umma_commit_w(&kv_empty_v[kvi & 1]);
             ++pv_it;
+            pv_last = s_it - 1;
             return true;
         };
         for (uint32_t i = 0; ok && !warp_flag(s_abort); ++i) {
@@ -336,48 +351,47 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             const MlaTcUnit U = mla_tc_unit(p, u, L);
             if (!mla_tc_unit_ok(p, U)) continue;
             ++q_it;  // units started (1-based below)
-            if (lane == 0) {
-                if (!mbar_wait(q_full, (q_it - 1) & 1, p.err) || !mbar_wait(qt_ready, (q_it - 1) & 1, p.err)) {
-                    ok = false;
-                } else {
-                    const uint32_t kv_base = kv_it;
-                    for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
-                        const int st = kv_it & 1;
-                        if (!mbar_wait(&kv_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
-                        if (s_it > 0 && !mbar_wait(s_free, (s_it - 1) & 1, p.err)) { ok = false; break; }
-                        tc_fence_after();
-                        if (U.half) issue_s_part(kv_it, std::integral_constant<int, 1>{}, std::integral_constant<int, 0>{});
-                        else issue_s_part(kv_it, std::integral_constant<int, 0>{}, std::integral_constant<int, 0>{});
-                        umma_commit(&kv_empty[st]);  // score-only chunks free once read
-                        // O += P . V of the previous tile goes between the two parts of
-                        // S: its value chunks are then released a whole S part earlier
-                        if (t > 0 && !issue_o(kv_it - 1, U.half, t == 1)) { ok = false; break; }
-                        if (!mbar_wait(&kv_full_v[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
-                        tc_fence_after();
-                        if (U.half) issue_s_part(kv_it, std::integral_constant<int, 1>{}, std::integral_constant<int, 1>{});
-                        else issue_s_part(kv_it, std::integral_constant<int, 0>{}, std::integral_constant<int, 1>{});
-                        umma_commit(s_full);
-                        ++s_it;
-                        if (t == U.ntiles - 1) umma_commit(q_empty);
-                    }
-                    if (ok && !issue_o(kv_base + U.ntiles - 1, U.half, U.ntiles == 1)) ok = false;
-                }
+            if (!mbar_wait_warp(q_full, (q_it - 1) & 1, p.err) || !mbar_wait_warp(qt_ready, (q_it - 1) & 1, p.err)) {
+                ok = false;
+                break;
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            kv_it = __shfl_sync(0xffffffffu, kv_it, 0);
+            const uint32_t kv_base = kv_it;
+            for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
+                const int st = kv_it & 1;
+                const uint32_t b = s_it & 1;  // S buffer of this tile
+                const uint32_t tS = tbase + kMtColS + b * kMtTile;
+                if (!mbar_wait_warp(&kv_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                // buffer b last held the P of tile s_it - 2: its P . V must be done
+                if (s_it >= 2 && !mbar_wait_warp(&pv_buf[b], ((s_it >> 1) - 1) & 1, p.err)) { ok = false; break; }
+                tc_fence_after();
+                if (U.half) issue_s_part(kv_it, tS, std::integral_constant<int, 1>{}, std::integral_constant<int, 0>{});
+                else issue_s_part(kv_it, tS, std::integral_constant<int, 0>{}, std::integral_constant<int, 0>{});
+                umma_commit_w(&kv_empty[st]);  // score-only chunks free once read
+                // O += P . V of the previous tile goes between the two parts of
+                // S: its value chunks are then released a whole S part earlier
+                if (t > 0 && !issue_o(kv_it - 1, U.half, t == 1, b ^ 1u)) { ok = false; break; }
+                if (!mbar_wait_warp(&kv_full_v[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                tc_fence_after();
+                if (U.half) issue_s_part(kv_it, tS, std::integral_constant<int, 1>{}, std::integral_constant<int, 1>{});
+                else issue_s_part(kv_it, tS, std::integral_constant<int, 0>{}, std::integral_constant<int, 1>{});
+                umma_commit_w(s_full);
+                ++s_it;
+                if (t == U.ntiles - 1) umma_commit_w(q_empty);
+            }
+            if (ok && !issue_o(kv_base + U.ntiles - 1, U.half, U.ntiles == 1, (s_it - 1) & 1u)) ok = false;
+            if (ok) umma_commit_w(o_full);
         }
         if (!ok) s_abort = 1;
-        // let every issued MMA finish before the CTA can exit
-        if (lane == 0 && pv_it > 0) mbar_wait(pv_done, (pv_it - 1) & 1, p.err);
-        __syncwarp();
+        // let every issued MMA finish before the CTA can exit: the last P . V
+        // (its buffer's earlier phases were all waited for above) covers them
+        if (pv_it > 0) mbar_wait_warp(&pv_buf[pv_last & 1], (pv_last >> 1) & 1, p.err);
     } else if (warp <= 5) {
         // ------------------------------------------------------------ softmax (one thread per head)
         const int hl = 32 * (warp & 3) + lane;  // head within the group = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tS = tbase + lane_off + kMtColS, tP = tbase + lane_off + kMtColP;
         const uint32_t tQ = tbase + lane_off + kMtColQ, tO = tbase + lane_off + kMtColO;
         const float sl2 = p.scale_log2;
-        uint32_t s_it = 0, pv_seen = 0;
+        uint32_t s_it = 0, o_seen = 0;
         for (uint32_t i = 0; !warp_flag(s_abort); ++i) {
             int u = 0;
             if (!take_unit(i, lane == 0, &u)) {
@@ -388,7 +402,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             const MlaTcUnit U = mla_tc_unit(p, u, L);
             if (!mla_tc_unit_ok(p, U)) continue;
             const int h = U.grp * 128 + hl;
-            // q[h, 0:320] -> TMEM. The previous unit's last S product, the
+            // q[h, 0:256] -> TMEM. The previous unit's last S product, the
             // only reader of these columns, is done: this warp saw its S.
             {
                 const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((int64_t)U.r * p.Hq + h) * kMtD);
@@ -415,6 +429,8 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             for (int t = 0; t < U.ntiles; ++t) {
                 if (!mbar_wait_warp(s_full, s_it & 1, p.err)) { ok = false; break; }
                 tc_fence_after();
+                // this tile's S buffer; its P goes over the first 32 columns
+                const uint32_t tS = tbase + lane_off + kMtColS + (s_it & 1) * kMtTile;
                 float s[kMtTile];
                 {
                     uint32_t r0[32], r1[32];
@@ -427,9 +443,6 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                         s[32 + k] = __uint_as_float(r1[k]);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_free);
                 ++s_it;
                 const int valid = min(kMtTile, U.k1 - (U.k0 + t * kMtTile));
                 if (valid < kMtTile) {
@@ -470,12 +483,8 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                     pk[k / 2] = pack_bf16(e0, e1);
                 }
                 l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                // the previous P . V must be done before P or O change
-                if (t > 0) {
-                    if (!mbar_wait_warp(pv_done, pv_seen & 1, p.err)) { ok = false; break; }
-                    ++pv_seen;
-                    tc_fence_after();
-                }
+                // O is free to rescale: the P . V of the previous tile was
+                // issued before this tile's S part 2, whose commit we waited for
                 // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp
                 // takes this branch if any of its heads needs the rescale (alpha
                 // stays 1 for the others)
@@ -490,7 +499,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                         tmem_st32(tO + c * 32, r);
                     }
                 }
-                tmem_st32(tP, pk);
+                tmem_st32(tS, pk);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -500,11 +509,11 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 s_abort = 1;
                 break;
             }
-            if (!mbar_wait_warp(pv_done, pv_seen & 1, p.err)) {
+            if (!mbar_wait_warp(o_full, o_seen & 1, p.err)) {
                 s_abort = 1;
                 break;
             }
-            ++pv_seen;
+            ++o_seen;
             tc_fence_after();
             // ---- epilogue: this half's 256 value dims of O / l
             const bool direct = p.nsplit[U.r] == 1;
