@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         const bool use_tma = p.bs >= 8;
         uint32_t kv_it = 0, q_it = 0;
         uint32_t last[2] = {0, 0};  // phase + 1 of this part's last copy per stage (0 = none)
+        int stage_half0 = -1, stage_half1 = -1;  // value half of the unit that last used stage 0 / 1
         for (uint32_t i = 0; !warp_flag(s_abort); ++i) {
             int u = 0;
             if (part == 0) {
@@ -251,6 +252,18 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                         ok = false;
                         break;
                     }
+                    // The parts are split by the unit's value half. After a unit of the
+                    // other half, this unit's score-only chunks are that unit's value
+                    // chunks, free only once its P . V has read them. (The value part
+                    // needs no such wait: its release comes after the previous tile's
+                    // whole S, score-only chunks included.)
+                    if (part == 0 && n > 0 && (st ? stage_half1 : stage_half0) != U.half &&
+                        !mbar_wait_warp(&kv_empty_v[st], (n - 1) & 1, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (st) stage_half1 = U.half;
+                    else stage_half0 = U.half;
                     if (tma) {
                         const int rows = p.bs < kMtTile ? p.bs : kMtTile;  // rows per box
                         const int nbox = kMtTile / rows;

@@ -116,6 +116,49 @@ def test_decode_mla_many_units():
     check_batch(W.make_batch(spec))
 
 
+def _repeat_bitwise(batch, steps):
+    """Run the same step `steps` times; every output must equal the first bit
+    for bit. Work units are taken dynamically, so the CTA that runs a unit,
+    and what ran on that CTA before it, changes from step to step: a race
+    between a unit and its predecessor on the same CTA shows up here even
+    when it stays inside the tolerance of a single comparison."""
+    import torch
+    from paged_kv_attention_07_gb300.device_batch import DeviceBatch
+    db = DeviceBatch(batch)
+    db.step()
+    torch.cuda.synchronize()
+    first_o, first_l = db.out.clone(), db.lse.clone()
+    for _ in range(steps):
+        db.step()
+        torch.cuda.synchronize()
+        assert torch.equal(db.out, first_o) and torch.equal(db.lse, first_l), "a repeated step changed the output"
+    assert db.error_word() == 0
+    out = first_o.float().cpu().numpy().reshape(-1, batch.spec.head_dim_v)
+    compare(batch, out, first_l.cpu().numpy().reshape(-1))
+
+
+def test_decode_mla_repeated_steps_bitwise():
+    # consecutive units of one CTA alternate value halves, whose latent
+    # chunks split into score-only and value parts differently
+    rng = np.random.default_rng(17)
+    ctx = rng.integers(1, 2500, 192).tolist()
+    _repeat_bitwise(W.make_batch(_dec("mla_rep", ctx, 128, 1, 576, 64, seed=17, mla=True, dv=512)), 24)
+
+
+@pytest.mark.parametrize("kind", ["gqa", "mixed"])
+def test_repeated_steps_bitwise(kind):
+    rng = np.random.default_rng(23)
+    if kind == "gqa":
+        ctx = rng.integers(1, 5000, 256).tolist()
+        batch = W.make_batch(_dec("gqa_rep", ctx, 32, 8, 128, 16, seed=23))
+    else:
+        spec = W.spec_custom("mixed_rep", ctx=[900, 3000, 40, 2000, 0, 0], qlen=[1, 1, 300, 77, 500, 129],
+                             num_decodes=2, num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=128, dv=128, bs=16,
+                             chunk=1024, seed=23)
+        batch = W.make_batch(spec)
+    _repeat_bitwise(batch, 12)
+
+
 def test_constant_v_gives_constant_output():
     spec = W.spec_custom("const", ctx=[0, 90, 30, 0], qlen=[1, 1, 20, 50], num_decodes=2,
                          num_extends=1, num_prefills=1, Hq=8, Hkv=2, d=128, dv=128, bs=16, chunk=32)
