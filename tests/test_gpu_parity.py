@@ -116,15 +116,17 @@ def test_decode_mla_many_units():
     check_batch(W.make_batch(spec))
 
 
-def _repeat_bitwise(batch, steps):
+def _repeat_bitwise(batch, steps, kv_scales=None):
     """Run the same step `steps` times; every output must equal the first bit
     for bit. Work units are taken dynamically, so the CTA that runs a unit,
     and what ran on that CTA before it, changes from step to step: a race
     between a unit and its predecessor on the same CTA shows up here even
-    when it stays inside the tolerance of a single comparison."""
+    when it stays inside the tolerance of a single comparison. The bf16 cases
+    also check the first output against the oracle (the 8-bit paths have
+    their own oracle tests)."""
     import torch
     from paged_kv_attention_07_gb300.device_batch import DeviceBatch
-    db = DeviceBatch(batch)
+    db = DeviceBatch(batch, kv_scales=kv_scales)
     db.step()
     torch.cuda.synchronize()
     first_o, first_l = db.out.clone(), db.lse.clone()
@@ -133,22 +135,25 @@ def _repeat_bitwise(batch, steps):
         torch.cuda.synchronize()
         assert torch.equal(db.out, first_o) and torch.equal(db.lse, first_l), "a repeated step changed the output"
     assert db.error_word() == 0
-    out = first_o.float().cpu().numpy().reshape(-1, batch.spec.head_dim_v)
-    compare(batch, out, first_l.cpu().numpy().reshape(-1))
+    if kv_scales is None:
+        out = first_o.float().cpu().numpy().reshape(-1, batch.spec.head_dim_v)
+        compare(batch, out, first_l.cpu().numpy().reshape(-1))
 
 
-def test_decode_mla_repeated_steps_bitwise():
+@pytest.mark.parametrize("bs", [64, 4])
+def test_decode_mla_repeated_steps_bitwise(bs):
     # consecutive units of one CTA alternate value halves, whose latent
-    # chunks split into score-only and value parts differently
+    # chunks split into score-only and value parts differently; block size
+    # 4 loads every tile by row gathers
     rng = np.random.default_rng(17)
     ctx = rng.integers(1, 2500, 192).tolist()
-    _repeat_bitwise(W.make_batch(_dec("mla_rep", ctx, 128, 1, 576, 64, seed=17, mla=True, dv=512)), 24)
+    _repeat_bitwise(W.make_batch(_dec("mla_rep", ctx, 128, 1, 576, bs, seed=17, mla=True, dv=512)), 24)
 
 
-@pytest.mark.parametrize("kind", ["gqa", "mixed"])
+@pytest.mark.parametrize("kind", ["gqa", "mixed", "gqa_fp8", "mixed_fp8"])
 def test_repeated_steps_bitwise(kind):
     rng = np.random.default_rng(23)
-    if kind == "gqa":
+    if kind.startswith("gqa"):
         ctx = rng.integers(1, 5000, 256).tolist()
         batch = W.make_batch(_dec("gqa_rep", ctx, 32, 8, 128, 16, seed=23))
     else:
@@ -156,7 +161,7 @@ def test_repeated_steps_bitwise(kind):
                              num_decodes=2, num_extends=2, num_prefills=2, Hq=16, Hkv=2, d=128, dv=128, bs=16,
                              chunk=1024, seed=23)
         batch = W.make_batch(spec)
-    _repeat_bitwise(batch, 12)
+    _repeat_bitwise(batch, 12, kv_scales=(0.0125, 0.02) if kind.endswith("fp8") else None)
 
 
 def test_constant_v_gives_constant_output():
