@@ -43,3 +43,23 @@ def test_two_gloo_ranks_take_the_slowest_time():
 def test_single_process_is_identity():
     assert bench.max_over_ranks(3.25) == 3.25
     assert bench.weak_scaling_value(1, 1.0e9, 1.0) == pytest.approx(1000.0)
+
+
+def test_launch_ranks_runs_torchrun_on_loopback(monkeypatch):
+    """bench.py --gpus N (outside torchrun) re-launches itself as N ranks of one
+    node, rendezvous on 127.0.0.1, and returns torchrun's exit code."""
+    seen = {}
+
+    def fake_call(cmd):
+        seen["cmd"] = cmd
+        return 3
+
+    monkeypatch.setattr(bench.subprocess, "call", fake_call)
+    rc = bench.launch_ranks(4, ["--gpus", "4", "--steps", "7"])
+    cmd = seen["cmd"]
+    assert rc == 3
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nnodes=1" in cmd and "--nproc-per-node=4" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert int(cmd[cmd.index("--master-port") + 1]) > 0
+    assert cmd[-5].endswith("bench.py") and cmd[-4:] == ["--gpus", "4", "--steps", "7"]
