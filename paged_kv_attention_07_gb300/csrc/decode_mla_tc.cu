@@ -104,7 +104,6 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     uint64_t* kv_full = bars + 0;     // [2] score-only chunks landed
     uint64_t* kv_empty = bars + 2;    // [2] score-only chunks read by S
     uint64_t* kv_full_v = bars + 16;  // [2] value chunks landed
-    uint64_t* kv_empty_v = bars + 18; // [2] value chunks read by S and P . V
     uint64_t* u_full = bars + 4;     // [2] unit ring slot written
     uint64_t* u_empty = bars + 6;    // [2] unit ring slot read by the issuer, the value producer and the 4 softmax warps
     uint64_t* q_full = bars + 8;     // q[:, 256:576] landed in shared memory
@@ -112,7 +111,10 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     uint64_t* qt_ready = bars + 10;  // q[:, 0:256] written to TMEM (4 warps)
     uint64_t* s_full = bars + 11;    // a tile's S complete (and the P . V issued before its part 2)
     uint64_t* p_full = bars + 13;    // 4 warps wrote P (and rescaled O)
-    uint64_t* pv_buf = bars + 20;    // [2] the P . V reading S buffer b complete: b free again
+    // [2] the P . V of the tiles using S buffer b complete: b is free again,
+    // and so are the value chunks of stage b (a tile's stage and S buffer are
+    // both its index in this CTA's tile sequence, mod 2)
+    uint64_t* pv_buf = bars + 20;
     uint64_t* o_full = bars + 22;    // a unit's last P . V complete
     uint64_t* o_free = bars + 15;    // 4 warps read O
     __shared__ uint32_t s_tmem;
@@ -129,7 +131,6 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
             mbar_init(&kv_full_v[i], 1);
-            mbar_init(&kv_empty_v[i], 1);
             mbar_init(&u_full[i], 1);
             mbar_init(&u_empty[i], 6);
         }
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 }
                 // part 0: the score-only chunks, part 1: the value chunks
                 {
-                    uint64_t* empty = part ? &kv_empty_v[st] : &kv_empty[st];
+                    uint64_t* empty = part ? &pv_buf[st] : &kv_empty[st];
                     uint64_t* full = part ? &kv_full_v[st] : &kv_full[st];
                     const uint32_t cmask = part ? vmask : (0x1FFu & ~vmask);
                     if (n > 0 && !mbar_wait_warp(empty, (n - 1) & 1, p.err)) {
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                     // needs no such wait: its release comes after the previous tile's
                     // whole S, score-only chunks included.)
                     if (part == 0 && n > 0 && (st ? stage_half1 : stage_half0) != U.half &&
-                        !mbar_wait_warp(&kv_empty_v[st], (n - 1) & 1, p.err)) {
+                        !mbar_wait_warp(&pv_buf[st], (n - 1) & 1, p.err)) {
                         ok = false;
                         break;
                     }
@@ -348,8 +349,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             for (int kk = 0; kk < kMtTile / 16; ++kk)
                 umma_bf16_ts_w(tbase + kMtColO, tbase + kMtColS + b * kMtTile + kk * 8,
                                umma_desc_sw128(v + kk * 16 * 128, kMtChunk, 1024), idesc_o, (!first || kk > 0) ? 1u : 0u);
-            umma_commit_w(&pv_buf[b]);
-            umma_commit_w(&kv_empty_v[kvi & 1]);
+            umma_commit_w(&pv_buf[b]);  // b == kvi & 1: also frees the stage's value chunks
             ++pv_it;
             pv_last = s_it - 1;
             return true;
@@ -369,11 +369,13 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 break;
             }
             const uint32_t kv_base = kv_it;
+            bool next_landed = false;  // the next tile's score-only chunks were seen complete
             for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
                 const int st = kv_it & 1;
                 const uint32_t b = s_it & 1;  // S buffer of this tile
                 const uint32_t tS = tbase + kMtColS + b * kMtTile;
-                if (!mbar_wait_warp(&kv_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                if (!next_landed && !mbar_wait_warp(&kv_full[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
+                next_landed = false;
                 // buffer b last held the P of tile s_it - 2: its P . V must be done
                 if (s_it >= 2 && !mbar_wait_warp(&pv_buf[b], ((s_it >> 1) - 1) & 1, p.err)) { ok = false; break; }
                 tc_fence_after();
@@ -383,6 +385,10 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 // O += P . V of the previous tile goes between the two parts of
                 // S: its value chunks are then released a whole S part earlier
                 if (t > 0 && !issue_o(kv_it - 1, U.half, t == 1, b ^ 1u)) { ok = false; break; }
+                // look (without blocking) at the next tile's score-only chunks now,
+                // while MMAs are queued, instead of waiting for them after part 2
+                if (t + 1 < U.ntiles)
+                    next_landed = __all_sync(0xffffffffu, mbar_test_wait(&kv_full[st ^ 1], ((kv_it + 1) >> 1) & 1));
                 if (!mbar_wait_warp(&kv_full_v[st], (kv_it >> 1) & 1, p.err)) { ok = false; break; }
                 tc_fence_after();
                 if (U.half) issue_s_part(kv_it, tS, std::integral_constant<int, 1>{}, std::integral_constant<int, 1>{});
