@@ -228,6 +228,18 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             };
             bool ok = true;
             const uint32_t vmask = U.half ? 0xF0u : 0x0Fu;  // chunks holding this half's value dims
+            // this part's chunks in order (gather path: a warp step takes two of
+            // them, one per half warp); entries past the count are -1
+            const uint32_t my_mask = part ? vmask : (0x1FFu & ~vmask);
+            int cl[6];
+            {
+                uint32_t m = my_mask;
+#pragma unroll
+                for (int j = 0; j < 6; ++j) {
+                    cl[j] = m ? __ffs(m) - 1 : -1;
+                    m &= m - 1;
+                }
+            }
             for (int t = 0; t < U.ntiles; ++t, ++kv_it) {
                 const int st = kv_it & 1;
                 const uint32_t n = kv_it >> 1;
@@ -235,12 +247,12 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 const int tb = U.k0 + t * kMtTile;
                 const int valid = min(kMtTile, U.k1 - tb);
                 const bool tma = use_tma && valid == kMtTile;
-                // gather path: lane l < 16 takes rows 4l .. 4l + 3 of the tile
+                // gather path: lanes l and l + 16 take rows 4l .. 4l + 3 of the tile
                 int grow[4] = {0, 0, 0, 0};
-                if (!tma && lane < kMtTile / 4) {
+                if (!tma) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const int pos = tb + 4 * lane + k;
+                        const int pos = tb + 4 * (lane & 15) + k;
                         grow[k] = pos < U.k1 ? block_of(pos) * p.bs + (pos % p.bs) : p.cache_rows;  // out of range: zeros
                     }
                 }
@@ -278,15 +290,18 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                                     tma_load_2d(dst + c * kMtChunk + lane * rows * 128, &kvmap, full, c * 64, row, pol);
                         }
                     } else {
-                        // TMA gathers, 4 rows x 64 dims per instruction, 16 lanes in
-                        // parallel; every chunk's bytes arrive (rows past the end as zeros)
+                        // TMA gathers, 4 rows x 64 dims per instruction, all 32 lanes in
+                        // parallel (two chunks per warp step); every chunk's bytes arrive
+                        // (rows past the end as zeros)
                         if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(__popc(cmask) * kMtChunk));
                         __syncwarp();
-                        if (lane < kMtTile / 4)
-                            for (int c = 0; c < 9; ++c)
-                                if ((cmask >> c) & 1)
-                                    tma_gather4(dst + c * kMtChunk + lane * 4 * 128, &gmap, full, c * 64, grow[0], grow[1],
-                                                grow[2], grow[3]);
+#pragma unroll
+                        for (int j = 0; j < 6; j += 2) {
+                            const int c = lane < 16 ? cl[j] : cl[j + 1];
+                            if (c >= 0)
+                                tma_gather4(dst + c * kMtChunk + (lane & 15) * 4 * 128, &gmap, full, c * 64, grow[0],
+                                            grow[1], grow[2], grow[3]);
+                        }
                     }
                 }
                 if (!ok) break;
