@@ -509,11 +509,43 @@ WORKLOADS = {"decode_gqa": W.spec_decode_gqa, "decode_gqa_fp8": W.spec_decode_gq
              "mla_decode_h64": lambda: W.spec_mla_decode(heads=64),
              "mla_prefill_extend_small": lambda: W.spec_mla_prefill(n_ext=2, n_pre=1, heads=32),
              "mla_decode_bs1": lambda: W.spec_mla_decode(block_size=1),
-             "mixed_unified": W.spec_mixed, "mixed_unordered": W.spec_mixed}
+             "mixed_unified": W.spec_mixed, "mixed_unordered": W.spec_mixed,
+             # the public two-input merge alone, on fp32 partials of the mixed
+             # batch's shape (every new token x 32 heads x 128 dims)
+             "merge_attn_states": W.spec_mixed}
+
+
+def profile_merge(args, device):
+    """pka_merge_attn_states on two fp32 partial outputs with their LSEs, one
+    row per (token, head) of the mixed batch: --steps timed calls."""
+    import torch
+    from paged_kv_attention_07_gb300 import pka
+    spec = WORKLOADS["merge_attn_states"]()
+    rows, dv = spec.num_tokens * spec.num_q_heads, spec.head_dim_v
+    g = torch.Generator(device=device).manual_seed(7)
+    a, b = (torch.randn(rows, dv, generator=g, device=device) for _ in range(2))
+    la, lb = (torch.randn(rows, generator=g, device=device) * 4 for _ in range(2))
+    out, lse = torch.empty_like(a), torch.empty_like(la)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        pka.pka_merge_attn_states(out, lse, a, la, b, lb)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in ev:
+        e0.record(stream)
+        pka.pka_merge_attn_states(out, lse, a, la, b, lb)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / args.steps
+    nbytes = rows * (3 * dv * 4 + 3 * 4)  # two partial rows and LSEs in, one row and LSE out
+    print(json.dumps({"workload": "merge_attn_states", "rows": rows, "head_dim": dv, "io": "fp32",
+                      "ms_per_call": ms, "gbs": round(nbytes / ms / 1e6, 1), "gpu_launches": args.steps}))
 
 
 def profile_workload(args, device):
     """Run --steps steps of one workload and print its timing (for profilers)."""
+    if args.workload == "merge_attn_states":
+        return profile_merge(args, device)
     spec = WORKLOADS[args.workload]()
     db = make_device_batch(spec, device, seed=7, unified=args.workload == "mixed_unified",
                            kv_scales=FP8_SCALES if args.workload.endswith("_fp8") else None)
